@@ -1,0 +1,341 @@
+"""Pins for the CPU oracle: checks against closed forms, special cases, brute force
+and hand-worked values — never against the oracle itself.
+
+Each test names the definition it pins (DFlash2 pages: the conv "inside each block",
+the selector's pairwise score and walk from the anchor; see the oracle's header).
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import core as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def bf16_of(values):
+    """bf16 bit patterns of values that are exactly representable in bf16."""
+    f = np.asarray(values, dtype=np.float32)
+    u = f.view(np.uint32)
+    assert np.all((u & 0xFFFF) == 0), "value not exact in bf16"
+    return (u >> 16).astype(np.uint16)
+
+
+# ---------------------------------------------------------------- storage rounding
+
+
+def test_round_bf16_known_patterns():
+    # 1, halfway cases (ties to even), just above halfway, negative, carry into exponent
+    cases = {
+        1.0: 0x3F80,
+        1.0 + 2.0 ** -8: 0x3F80,              # halfway between 0x3F80 and 0x3F81 -> even
+        1.0 + 3 * 2.0 ** -8: 0x3F82,          # halfway between 0x3F81 and 0x3F82 -> even
+        1.0 + 2.0 ** -8 + 2.0 ** -40: 0x3F81,  # just above halfway -> up
+        -2.5: 0xC020,
+        2.0 - 2.0 ** -9: 0x4000,              # rounds up across the binade
+        0.0: 0x0000,
+        3.0e38: 0x7F62,
+    }
+    got = O.round_bf16(np.array(list(cases.keys())))
+    assert [int(g) for g in got] == list(cases.values())
+
+
+def test_round_bf16_matches_torch_on_fp32_values():
+    # values exact in fp32 round the same way from double and from float (no double rounding)
+    rng = np.random.default_rng(0)
+    x = (rng.standard_normal(200_000) * 3).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(O.round_bf16(x.astype(np.float64)), ref)
+
+
+# ---------------------------------------------------------------- conv (kernel size 2)
+
+
+def _pos_hidden(B, T, H, seed=0):
+    rng = np.random.default_rng(seed)
+    q = rng.integers(1, 32, size=(B, T, H)) / 4.0  # positive multiples of 1/4: exact in bf16
+    return bf16_of(q)
+
+
+def test_conv_zero_weights_is_pairwise_mean():
+    # zero projection -> taps (1/2, 1/2): y[t] = (x[t] + x[t-1]) / 2, y[0] = x[0] / 2
+    B, T, H = 2, 5, 32
+    rng = np.random.default_rng(1)
+    xq = rng.integers(-32, 33, size=(B, T, H)) / 4.0
+    x = bf16_of(xq)
+    w = np.zeros((1, 2 * H // 16, H), dtype=np.uint16)
+    z = O.widen(O.conv_chain(x, w, "bf16", 16))
+    exp = np.empty_like(xq)
+    exp[:, 0] = xq[:, 0] / 2
+    exp[:, 1:] = (xq[:, 1:] + xq[:, :-1]) / 2
+    assert np.array_equal(z, exp)
+
+
+def _tap_weights(H, group_size, mode_per_group, mag=8.0):
+    """mode 'shift': tap 0 huge -> y = x[t-1]; mode 'id': tap 1 huge -> y = x[t]."""
+    G = H // group_size
+    w = np.zeros((2 * G, H), dtype=np.float32)
+    for g in range(G):
+        s = 1.0 if mode_per_group(g) == "shift" else -1.0
+        w[2 * g, :] = s * mag
+        w[2 * g + 1, :] = -s * mag
+    return bf16_of(w)
+
+
+@pytest.mark.parametrize("layers", [1, 2, 3, 5])
+def test_conv_shift_limit_chains_layers(layers):
+    # all taps select x[t-1]: after L layers z[t] = x[t-L] (zero for t < L)
+    B, T, H = 2, 8, 64
+    x = _pos_hidden(B, T, H)
+    w1 = _tap_weights(H, 16, lambda g: "shift")
+    w = np.stack([w1] * layers)
+    z = O.widen(O.conv_chain(x, w, "bf16", 16))
+    xf = O.widen(x)
+    exp = np.zeros_like(xf)
+    exp[:, layers:] = xf[:, :T - layers]
+    assert np.array_equal(z, exp)
+
+
+def test_conv_identity_limit():
+    B, T, H = 1, 4, 64
+    x = _pos_hidden(B, T, H, seed=3)
+    w = _tap_weights(H, 16, lambda g: "id")[None]
+    assert np.array_equal(O.conv_chain(x, w, "bf16", 16), x)
+
+
+def test_conv_group_mapping_sixteen_channels_per_group():
+    # even groups shift, odd groups pass through: channel c follows group c // 16
+    B, T, H = 1, 6, 96
+    x = _pos_hidden(B, T, H, seed=4)
+    w = _tap_weights(H, 16, lambda g: "shift" if g % 2 == 0 else "id")[None]
+    z = O.widen(O.conv_chain(x, w, "bf16", 16))
+    xf = O.widen(x)
+    for c in range(H):
+        if (c // 16) % 2 == 0:
+            assert np.array_equal(z[0, 0, c], 0.0) and np.array_equal(z[0, 1:, c], xf[0, :-1, c])
+        else:
+            assert np.array_equal(z[0, :, c], xf[0, :, c])
+
+
+def test_conv_raw_taps_constant_projection():
+    # channel 0 is 1 everywhere; projection rows read only channel 0 -> raw taps (alpha, beta)
+    # so y = alpha * x[t-1] + beta * x[t] for every channel
+    B, T, H, gs = 1, 5, 32, 16
+    rng = np.random.default_rng(5)
+    xq = rng.integers(-16, 17, size=(B, T, H)) / 4.0
+    xq[..., 0] = 1.0
+    alpha, beta = 0.5, 0.25
+    w = np.zeros((2 * H // gs, H), dtype=np.float32)
+    w[0::2, 0] = alpha
+    w[1::2, 0] = beta
+    z = O.conv_chain(bf16_of(xq), bf16_of(w)[None], "bf16", gs, taps="raw")
+    exp = beta * xq
+    exp[:, 1:] += alpha * xq[:, :-1]
+    assert np.array_equal(O.widen(z), exp)
+
+
+def test_conv_causal_and_convex():
+    rc = synth.recipe(2)
+    sh = synth.Shape(batch=2, block=8, hidden=256, vocab=64, top_k=4, rank=32, layers=3)
+    r = synth.Recipe(seed=11, shape=sh, rms_normalise=True, conv_std=0.05)
+    inp = synth.make_inputs(r)
+    z = O.conv_chain(inp["hidden"], inp["conv_w"], "bf16", 16)
+    h2 = inp["hidden"].copy()
+    h2[:, 5:] = synth.f64_to_bf16(np.full(h2[:, 5:].shape, 3.0))  # change positions 5..7 only
+    z2 = O.conv_chain(h2, inp["conv_w"], "bf16", 16)
+    assert np.array_equal(z[:, :5], z2[:, :5])
+    assert not np.array_equal(z[:, 5:], z2[:, 5:])
+    # one layer: |y[t]| <= max(|x[t]|, |x[t-1]|) elementwise (convex combination)
+    z1 = O.widen(O.conv_chain(inp["hidden"], inp["conv_w"][:1], "bf16", 16))
+    x = O.widen(inp["hidden"])
+    xp = np.zeros_like(x)
+    xp[:, 1:] = x[:, :-1]
+    assert np.all(np.abs(z1) <= np.maximum(np.abs(x), np.abs(xp)))
+    del rc
+
+
+# ---------------------------------------------------------------- logits, lse, top-K
+
+
+def test_logits_hand_case_and_orientation():
+    z = bf16_of([[1.0, 2.0]])
+    W = bf16_of([[3.0, 4.0], [5.0, 6.0], [-1.0, 0.0]])
+    assert O.logits(z, W).tolist() == [[11.0, 17.0, -1.0]]
+    # one-hot lm_head rows gather the hidden channel: l[m, v] = z[m, v mod H]
+    H, Vv = 48, 200
+    rng = np.random.default_rng(6)
+    zq = bf16_of(rng.integers(-64, 64, size=(3, H)) / 8.0)
+    Wq = np.zeros((Vv, H), dtype=np.float32)
+    Wq[np.arange(Vv), np.arange(Vv) % H] = 1.0
+    l = O.logits(zq, bf16_of(Wq), chunk=64)
+    assert np.array_equal(l, O.widen(zq)[:, np.arange(Vv) % H].astype(np.float32))
+
+
+def test_lse_closed_forms():
+    Vv = 248320
+    l = np.full((1, Vv), 2.5, dtype=np.float32)
+    assert abs(O.logsumexp_rows(l)[0] - (2.5 + math.log(Vv))) < 1e-9
+    # two values: n copies of a, the rest b
+    n, a, b = 17, 4.0, -1.0
+    l = np.full((1, 1000), b, dtype=np.float32)
+    l[0, :n] = a
+    exp = math.log(n * math.exp(a) + (1000 - n) * math.exp(b))
+    assert abs(O.logsumexp_rows(l)[0] - exp) < 1e-12
+    # cand log-prob of uniform logits is -log V
+    lp = O.cand_logprob(np.full((1, 4), 2.5, np.float32), np.array([2.5 + math.log(Vv)]))
+    assert np.allclose(lp, -math.log(Vv), atol=1e-6)
+
+
+def test_topk_ties_to_lower_id_closed_form():
+    # l[v] = -(v mod 7): the 0-valued ids are the multiples of 7, in id order
+    Vv, K = 4133, 16
+    l = (-(np.arange(Vv) % 7)).astype(np.float32)[None]
+    ids, vals, nxt = O.topk_rows(l, K)
+    assert ids[0].tolist() == [7 * i for i in range(K)]
+    assert np.all(vals == 0) and nxt[0] == 0
+    # mixed values: compare with an independent ordering (Python's sort on (-value, id))
+    rng = np.random.default_rng(7)
+    l = (rng.integers(-20, 20, size=(5, 3000)) / 4.0).astype(np.float32)
+    ids, vals, _ = O.topk_rows(l, 16)
+    for m in range(5):
+        ref = sorted(range(3000), key=lambda v: (-float(l[m, v]), v))[:16]
+        assert ids[m].tolist() == ref
+
+
+# ---------------------------------------------------------------- transitions
+
+
+def test_transitions_roles_of_u_and_v():
+    # U[v] = e_{v mod R}, V[v] = 2 e_{(v+1) mod R}: tau(i, j) = 2 [prev_i mod R == (cur_j + 1) mod R]
+    R, Vv, B, T, K = 8, 64, 2, 3, 4
+    U = np.zeros((Vv, R), np.float32)
+    V = np.zeros((Vv, R), np.float32)
+    U[np.arange(Vv), np.arange(Vv) % R] = 1.0
+    V[np.arange(Vv), (np.arange(Vv) + 1) % R] = 2.0
+    rng = np.random.default_rng(8)
+    cand = rng.integers(0, Vv, size=(B, T, K)).astype(np.int32)
+    anchor = rng.integers(0, Vv, size=B).astype(np.int32)
+    tau = O.transitions(anchor, cand, bf16_of(U), bf16_of(V))
+    for b in range(B):
+        for t in range(T):
+            for i in range(K):
+                prev = anchor[b] if t == 0 else cand[b, t - 1, i]
+                for j in range(K):
+                    exp = 2.0 if prev % R == (cand[b, t, j] + 1) % R else 0.0
+                    assert tau[b, t, i, j] == exp
+
+
+# ---------------------------------------------------------------- Viterbi
+
+
+def _golden_case(c):
+    K = len(c["cand_lp"][0])
+    T = len(c["cand_lp"])
+    lp = np.asarray(c["cand_lp"], np.float32)[None]
+    tau = np.zeros((1, T, K, K), np.float32)
+    tau[0, 0, :, :] = np.asarray(c["tau0"], np.float32)[None, :]
+    for t in range(1, T):
+        tau[0, t] = np.asarray(c["tau"][t - 1], np.float32)
+    return lp, tau
+
+
+def test_viterbi_hand_worked_golden():
+    with open(os.path.join(GOLDEN, "viterbi_hand.json")) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        lp, tau = _golden_case(c)
+        path, score = O.viterbi(lp, tau)
+        assert path[0].tolist() == c["viterbi_path"] and float(score[0]) == c["viterbi_score"]
+        gp, gs = O.greedy_walk(lp, tau)
+        assert gp[0].tolist() == c["greedy_path"] and float(gs[0]) == c["greedy_score"]
+        best, second = O.viterbi_two_best(lp, tau)
+        assert best[0] == c["viterbi_score"] and second[0] == c["second_best"]
+
+
+@pytest.mark.parametrize("K,T", [(4, 4), (3, 6), (16, 3), (2, 9)])
+def test_viterbi_equals_brute_force(K, T):
+    rng = np.random.default_rng(K * 100 + T)
+    B = 3
+    lp = (-np.abs(rng.standard_normal((B, T, K))) * 2).astype(np.float32)
+    lp = -np.sort(-lp, axis=2)
+    tau = (rng.standard_normal((B, T, K, K))).astype(np.float32)
+    tau[:, 0] = tau[:, 0, :1]  # slot 0: one predecessor (the anchor)
+    path, score = O.viterbi(lp, tau)
+    bp, bs = O.brute_force_best(lp, tau)
+    assert np.array_equal(path, bp)
+    assert np.allclose(score, bs, atol=1e-5)
+    assert np.allclose(O.path_score(lp, tau, path), score, atol=1e-5)
+    best, second = O.viterbi_two_best(lp, tau)
+    assert np.allclose(best, bs, atol=1e-9)
+    # the second best by enumeration
+    import itertools
+    for b in range(B):
+        allv = sorted((O.path_score(lp[b:b + 1], tau[b:b + 1], np.asarray(c)[None])[0]
+                       for c in itertools.product(range(K), repeat=T)), reverse=True)
+        assert abs(allv[1] - second[b]) < 1e-9
+    gp, gs = O.greedy_walk(lp, tau)
+    assert np.all(gs <= bs + 1e-9)
+
+
+def test_viterbi_zero_transitions_is_per_slot_argmax():
+    rng = np.random.default_rng(9)
+    lp = -np.sort(np.abs(rng.standard_normal((4, 8, 16))), axis=2).astype(np.float32)
+    tau = np.zeros((4, 8, 16, 16), np.float32)
+    path, score = O.viterbi(lp, tau)
+    assert np.all(path == 0)  # sorted candidates: candidate 0 is each slot's argmax
+    assert np.allclose(score, lp[:, :, 0].astype(np.float64).sum(axis=1), atol=1e-5)
+
+
+def test_viterbi_invariant_to_per_slot_constants():
+    rng = np.random.default_rng(10)
+    lp = rng.standard_normal((3, 6, 5)).astype(np.float32)
+    tau = rng.standard_normal((3, 6, 5, 5)).astype(np.float32)
+    tau[:, 0] = tau[:, 0, :1]
+    shift = (rng.integers(-8, 8, size=(3, 6, 1)) * 4.0).astype(np.float32)
+    p1, _ = O.viterbi(lp, tau)
+    p2, _ = O.viterbi(lp + shift, tau)
+    assert np.array_equal(p1, p2)
+
+
+def test_viterbi_single_slot_and_exact_ties():
+    rng = np.random.default_rng(12)
+    lp = rng.standard_normal((2, 1, 6)).astype(np.float32)
+    tau = rng.standard_normal((2, 1, 6, 6)).astype(np.float32)
+    tau[:, 0] = tau[:, 0, :1]
+    path, score = O.viterbi(lp, tau)
+    for b in range(2):
+        assert path[b, 0] == int(np.argmax(lp[b, 0] + tau[b, 0, 0]))
+    # all-equal scores: every argmax takes the lowest index
+    lp = np.ones((1, 5, 4), np.float32)
+    tau = np.ones((1, 5, 4, 4), np.float32)
+    path, score = O.viterbi(lp, tau)
+    assert np.all(path == 0) and float(score[0]) == 10.0
+
+
+# ---------------------------------------------------------------- whole tail
+
+
+def test_tiny_fp32_workload_end_to_end_brute_force():
+    rc = synth.recipe(1)
+    sh = rc.shape
+    inp = synth.make_inputs(rc)
+    out = O.draft_tail(inp, sh)
+    # every selected id is one of that slot's candidates, and the walk is the exact best path
+    bp, bs = O.brute_force_best(out["cand_lp"], out["tau"])
+    assert np.array_equal(bp, out["path_idx"])
+    assert np.allclose(bs, out["score"], atol=1e-5)
+    # the candidates are the true top-4 of a direct dot-product evaluation of a few rows
+    z = O.widen(out["z"]).reshape(-1, sh.hidden)
+    W = inp["lm_head"].astype(np.float64)
+    for m in range(z.shape[0]):
+        direct = np.array([float(np.dot(z[m], W[v])) for v in range(sh.vocab)], dtype=np.float32)
+        ref = sorted(range(sh.vocab), key=lambda v: (-float(direct[v]), v))[:sh.top_k]
+        assert out["cand_ids"].reshape(-1, sh.top_k)[m].tolist() == ref
+        lse = math.log(sum(math.exp(float(x)) for x in direct))
+        assert abs(out["lse"].reshape(-1)[m] - lse) < 1e-9
+    assert out["best"][0] >= out["second"][0]
