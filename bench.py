@@ -1,0 +1,490 @@
+#!/usr/bin/env python
+"""Benchmark of the DFlash2 draft tail on GB300: draft blocks/s and µs per call.
+
+One step = one dflash2_draft_tail call (5 conv layers -> LM-head contraction with fused
+top-16 + log-sum-exp -> merge -> transitions + Viterbi) over one batch of the page-shape
+workload (block 8, hidden 5120, vocab 248,320, K=16, rank 256), inputs resident in HBM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Device timing: the call is captured in a CUDA graph; before every step a 256 MiB buffer is
+written to flush L2 (129 MB), then the step is bracketed by CUDA events on its stream.
+The dominant kernel (the LM-head contraction) is timed the same way on its own for the
+roofline. `e2e` times the public call with pinned host buffers: the step's inputs
+(hidden, anchor) copied in and its results (path ids, path indices, scores) copied out
+inside the timed region. Under torchrun every rank runs its own replica (replicas only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "draft blocks/s (B=1, block 8, hidden 5120, vocab 248320, K=16, rank 256, 5 conv layers)"
+UNIT = "blocks/s"
+FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=2, help="workload (2: B=1 page shape)")
+    ap.add_argument("--no-extra", action="store_true", help="skip the B=8/B=32 lines and the CPU baseline")
+    ap.add_argument("--kernel", choices=["lmhead"], default=None,
+                    help="time one kernel alone (profiling case) instead of the whole tail")
+    ap.add_argument("--rows", type=int, default=8, help="--kernel: rows of the contraction")
+    ap.add_argument("--vocab", type=int, default=62080, help="--kernel: vocabulary size")
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+# ---------------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.path = tempfile.mktemp(prefix="dflash2_clocks_", suffix=".csv")
+        self.proc = None
+        self.marks = []
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu=timestamp,{self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "20"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def mark(self):
+        self.marks.append(time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append(dict(ts=ts, index=int(parts[1]), sm=float(parts[2]), smax=float(parts[3]),
+                                 hw=parts[6], hwt=parts[7], swt=parts[8], swp=parts[9]))
+            except Exception:
+                continue
+        os.unlink(self.path)
+        mine = [r for r in rows if r["index"] == self.index] or rows
+        if len(self.marks) >= 2:
+            t0, t1 = self.marks[0] - 0.05, self.marks[-1] + 0.05
+            inside = [r for r in mine if t0 <= r["ts"] <= t1]
+            mine = inside or mine
+        if not mine:
+            return None
+        reasons = set()
+        for r in mine:
+            for k, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"), ("swt", "sw_thermal_slowdown"),
+                            ("swp", "sw_power_cap")):
+                if r[k].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in mine), "sm_max_mhz": max(r["smax"] for r in mine),
+                "reasons": sorted(reasons), "samples": len(mine)}
+
+
+# ---------------------------------------------------------------------------------- workload
+
+def make_workload(config: int):
+    import synth
+    rc = synth.recipe(config)
+    inp = synth.make_inputs(rc)
+    return rc, inp
+
+
+def hidden_for_batch(rc, batch: int, lm_head):
+    """Hidden rows for another batch size with the same recipe (weights shared)."""
+    import synth
+    r2 = synth.scaled_recipe(rc, batch=batch)
+    r2.seed = rc.seed + 100 + batch
+    h = synth.normal(r2.seed, synth.TID_HIDDEN, (batch, rc.shape.block, rc.shape.hidden), 1.0, "f64")
+    h = h / np.sqrt(np.mean(h * h, axis=-1, keepdims=True) + 1e-6)
+    anchor = synth.uniform_int(r2.seed, synth.TID_ANCHOR, batch, rc.shape.vocab).astype(np.int32)
+    return synth.f64_to_bf16(h), anchor
+
+
+def lmhead_alg_bytes(sh, M):
+    """Algorithmic bytes of one LM-head contraction launch: the weight stream, the rows,
+    and the partials written (per-partition top-16 + (max, sum) per row)."""
+    return sh.vocab * sh.hidden * 2 + M * sh.hidden * 2
+
+
+def tail_roofline_us(sh, M, bw_gbs, tflops):
+    flop = 2.0 * M * sh.hidden * sh.vocab
+    return max(flop / (tflops * 1e12), sh.vocab * sh.hidden * 2 / (bw_gbs * 1e9)) * 1e6
+
+
+def traffic_record(kind: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current
+    kernel source (hash match); otherwise None."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "lmhead_traffic.json")) as f:
+            rec = json.load(f)
+        src = os.path.join(ROOT, "block_drafter_dflash2_gb300", "csrc")
+        h = hashlib.sha256()
+        for name in ("tc_gemm.cuh", "ptx.cuh", "lmhead_tc.cu"):
+            h.update(open(os.path.join(src, name), "rb").read())
+        if rec.get("source_sha256") != h.hexdigest():
+            return None
+        return rec.get(kind)
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------------- ours
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import block_drafter_dflash2_gb300 as df2
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    df2.load()
+    bw, tf, peak_kind = peaks()
+    rc, inp = make_workload(args.config)
+    sh = rc.shape
+    B, T, H, K = sh.batch, sh.block, sh.hidden, sh.top_k
+    M = B * T
+
+    def up(a):
+        if a.dtype == np.uint16:
+            a = a.view(np.int16)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    d = {k: up(inp[k]) for k in ("hidden", "lm_head", "U", "V", "conv_w", "anchor")}
+    shape = df2.Shape.make(B, T, H, sh.vocab, K, sh.rank, sh.layers)
+    ws = torch.zeros(df2.workspace_size(shape), dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    out = dict(pid=torch.empty((B, T), dtype=torch.int32, device=dev),
+               pix=torch.empty((B, T), dtype=torch.int32, device=dev),
+               score=torch.empty((B,), dtype=torch.float32, device=dev))
+    stream = torch.cuda.Stream(device=dev)
+
+    def call(hidden, anchor, shp=shape, o=out, s=stream):
+        df2.draft_tail(shp, hidden, d["lm_head"], d["U"], d["V"], d["conv_w"], anchor, o["pid"], o["pix"],
+                       o["score"], ws, stream=s)
+
+    def timed(fn, steps, warm):
+        """Per-step device time (ms) of fn on `stream`, L2 flushed before every step."""
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        with torch.cuda.stream(stream):
+            for _ in range(warm):
+                flush.fill_(1)
+                fn()
+            torch.cuda.synchronize(dev)
+            for e0, e1 in evs:
+                flush.fill_(1)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+            torch.cuda.synchronize(dev)
+        return [e0.elapsed_time(e1) for e0, e1 in evs]
+
+    # correctness of the captured call before timing it
+    with torch.cuda.stream(stream):
+        call(d["hidden"], d["anchor"])
+    torch.cuda.synchronize(dev)
+    assert df2.read_device_error(ws, stream) == 0, "device error word set"
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        call(d["hidden"], d["anchor"])
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.fill_(1)
+            graph.replay()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.mark()
+    step_ms = timed(graph.replay, args.steps, 0)
+    clocks.mark()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = sum(step_ms)
+    t_max = total_ms
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        t_max = float(t.item())
+    clk = clocks.stop()
+
+    # dominant kernel on its own: the LM-head contraction with its fused epilogue
+    z = torch.empty_like(d["hidden"])
+    df2.conv(shape, d["hidden"], d["conv_w"], z, ws, stream=stream)
+    lm_ms = timed(lambda: df2.lmhead_partials(shape, z, d["lm_head"], ws, stream=stream), args.steps, 3)
+    conv_ms = timed(lambda: df2.conv(shape, d["hidden"], d["conv_w"], z, ws, stream=stream), min(args.steps, 50), 3)
+    ids = torch.empty((M, K), dtype=torch.int32, device=dev)
+    lp = torch.empty((M, K), dtype=torch.float32, device=dev)
+    merge_ms = timed(lambda: df2.merge_partials(shape, ids, lp, None, ws, stream=stream), min(args.steps, 50), 3)
+    walk_ms = timed(lambda: df2.viterbi(shape, d["anchor"], ids, lp, d["U"], d["V"], out["pid"], out["pix"],
+                                        out["score"], ws, stream=stream), min(args.steps, 50), 3)
+
+    # end to end through the public call, host buffers in and out
+    h_hidden = torch.from_numpy(inp["hidden"].view(np.int16)).pin_memory()
+    h_anchor = torch.from_numpy(inp["anchor"]).pin_memory()
+    h_pid = torch.empty((B, T), dtype=torch.int32).pin_memory()
+    h_pix = torch.empty((B, T), dtype=torch.int32).pin_memory()
+    h_score = torch.empty((B,), dtype=torch.float32).pin_memory()
+    d_hidden = torch.empty_like(d["hidden"])
+    d_anchor = torch.empty_like(d["anchor"])
+
+    def e2e_step():
+        d_hidden.copy_(h_hidden, non_blocking=True)
+        d_anchor.copy_(h_anchor, non_blocking=True)
+        call(d_hidden, d_anchor)
+        h_pid.copy_(out["pid"], non_blocking=True)
+        h_pix.copy_(out["pix"], non_blocking=True)
+        h_score.copy_(out["score"], non_blocking=True)
+
+    e2e_ms = timed(e2e_step, args.steps, 3)
+    assert np.array_equal(h_pid.numpy(), out["pid"].cpu().numpy())
+    e2e_total = sum(e2e_ms)
+    if world > 1:
+        t = torch.tensor([e2e_total], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_total = float(t.item())
+
+    # other batch sizes of the metric (weights shared with the main workload)
+    extra = {}
+    if not args.no_extra and world == 1:
+        for b2 in (8, 32):
+            hb, ab = hidden_for_batch(rc, b2, inp["lm_head"])
+            hb_d, ab_d = up(hb), up(ab)
+            shp2 = df2.Shape.make(b2, T, H, sh.vocab, K, sh.rank, sh.layers)
+            ws2 = torch.zeros(df2.workspace_size(shp2), dtype=torch.uint8, device=dev)
+            o2 = dict(pid=torch.empty((b2, T), dtype=torch.int32, device=dev),
+                      pix=torch.empty((b2, T), dtype=torch.int32, device=dev),
+                      score=torch.empty((b2,), dtype=torch.float32, device=dev))
+
+            def call2(shp2=shp2, o2=o2, ws2=ws2, hb_d=hb_d, ab_d=ab_d):
+                df2.draft_tail(shp2, hb_d, d["lm_head"], d["U"], d["V"], d["conv_w"], ab_d, o2["pid"], o2["pix"],
+                               o2["score"], ws2, stream=stream)
+            with torch.cuda.stream(stream):
+                call2()
+            torch.cuda.synchronize(dev)
+            assert df2.read_device_error(ws2, stream) == 0
+            g2 = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g2, stream=stream):
+                call2()
+            ms2 = timed(g2.replay, args.steps, 3)
+            z2 = torch.empty_like(hb_d)
+            df2.conv(shp2, hb_d, d["conv_w"], z2, ws2, stream=stream)
+            lm2 = timed(lambda: df2.lmhead_partials(shp2, z2, d["lm_head"], ws2, stream=stream), args.steps, 3)
+            us = statistics.mean(ms2) * 1e3
+            lmu = statistics.mean(lm2) * 1e3
+            roof = tail_roofline_us(sh, b2 * T, bw, tf)
+            extra[f"B={b2}"] = {
+                "us_per_call": round(us, 2), "blocks_per_s": round(b2 / (us * 1e-6), 1),
+                "tail_roofline_frac": round(roof / us, 4), "lmhead_us": round(lmu, 2),
+                "lmhead_hbm_gbs": round(lmhead_alg_bytes(sh, b2 * T) / (lmu * 1e-6) / 1e9, 1),
+                "lmhead_tflops": round(2.0 * b2 * T * H * sh.vocab / (lmu * 1e-6) / 1e12, 1)}
+
+    us = total_ms / args.steps * 1e3
+    lm_us = statistics.mean(lm_ms) * 1e3
+    achieved = lmhead_alg_bytes(sh, M) / (lm_us * 1e-6) / 1e9
+    value = world * B * args.steps / (t_max * 1e-3)
+    e2e_val = world * B * args.steps / (e2e_total * 1e-3)
+    launches_per_step = sh.layers + 3
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t_max / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded Philox inputs, random weights)",
+        "config": {"workload": rc.name, "batch": B, "block": T, "hidden": H, "vocab": sh.vocab, "top_k": K,
+                   "rank": sh.rank, "conv_layers": sh.layers, "parallelism": "replicas" if world > 1 else "single",
+                   "timing": "CUDA graph replay, CUDA events per step",
+                   "l2": "flushed before every step (256 MiB write)"},
+        "us_per_call": round(us, 2),
+        "us_per_call_p10_p90": [round(float(np.percentile(step_ms, 10)) * 1e3, 2),
+                                round(float(np.percentile(step_ms, 90)) * 1e3, 2)],
+        "tail_roofline_frac": round(tail_roofline_us(sh, M, bw, tf) / us, 4),
+        "stages_us": {"conv_5_layers": round(statistics.mean(conv_ms) * 1e3, 2), "lmhead": round(lm_us, 2),
+                      "merge": round(statistics.mean(merge_ms) * 1e3, 2),
+                      "transition_walk": round(statistics.mean(walk_ms) * 1e3, 2)},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": bw, "unit": "GB/s",
+                     "frac": round(achieved / bw, 4), "traffic": traffic_record(f"M={M}"),
+                     "kernel": "tc_gemm_kernel<EpiTopK> (LM-head contraction + fused top-16/lse)",
+                     "peak_source": f"{peak_kind} hbm_gbs"},
+        "e2e": {"value": round(e2e_val, 2), "unit": UNIT,
+                "h2d_bytes_per_step": int(inp["hidden"].nbytes + inp["anchor"].nbytes),
+                "d2h_bytes_per_step": int(h_pid.numel() * 4 + h_pix.numel() * 4 + h_score.numel() * 4),
+                "us_per_call": round(e2e_total / args.steps * 1e3, 2)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "also": extra,
+    }
+    return line, rc, inp
+
+
+def run_kernel_case(args):
+    """Profiling case: the LM-head contraction with its fused epilogue alone, on `rows` page-shape
+    rows and a `vocab`-row head (default 62,080 rows = 636 MB, larger than L2)."""
+    import torch
+    import synth
+    import block_drafter_dflash2_gb300 as df2
+    df2.load()
+    dev = torch.device("cuda", 0)
+    rc = synth.scaled_recipe(synth.recipe(2), batch=args.rows, block=1, vocab=args.vocab, layers=0)
+    sh = rc.shape
+    inp = synth.make_inputs(rc)
+    z = torch.from_numpy(inp["hidden"].view(np.int16)).to(dev)
+    w = torch.from_numpy(inp["lm_head"].view(np.int16)).to(dev)
+    shape = df2.Shape.make(args.rows, 1, sh.hidden, sh.vocab, sh.top_k, sh.rank, 0)
+    ws = torch.zeros(df2.workspace_size(shape), dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    ms = []
+    for i in range(args.warmup + args.steps):
+        flush.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        df2.lmhead_partials(shape, z, w, ws)
+        e1.record()
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            ms.append(e0.elapsed_time(e1))
+    assert df2.read_device_error(ws) == 0
+    us = statistics.mean(ms) * 1e3
+    print(json.dumps({"kernel": "lmhead_partials", "rows": args.rows, "vocab": sh.vocab, "hidden": sh.hidden,
+                      "us": round(us, 2), "alg_gbs": round(lmhead_alg_bytes(sh, args.rows) / (us * 1e-6) / 1e9, 1),
+                      "tflops": round(2.0 * args.rows * sh.hidden * sh.vocab / (us * 1e-6) / 1e12, 1)}), flush=True)
+
+
+# ---------------------------------------------------------------------------------- oracle
+
+def oracle_shard_step(rc, inp, shard: int, n_shards: int):
+    """One bounded sample of the workload for the CPU oracle: the whole tail (conv, logits,
+    lse, full-sort top-K, transitions, Viterbi) on vocabulary shard `shard` of `n_shards`."""
+    from oracle import core as O
+    import synth
+    sh = rc.shape
+    Vs = sh.vocab // n_shards
+    v0 = shard * Vs
+    sub = dict(inp)
+    sub["lm_head"] = inp["lm_head"][v0:v0 + Vs]
+    sub["U"] = inp["U"][v0:v0 + Vs]
+    sub["V"] = inp["V"][v0:v0 + Vs]
+    sub["anchor"] = (np.asarray(inp["anchor"]) % Vs).astype(np.int32)
+    sh2 = synth.Shape(**{**sh.__dict__, "vocab": Vs})
+    return O.draft_tail(sub, sh2)
+
+
+def cpu_baseline(rc, inp, n_shards=1):
+    t0 = time.perf_counter()
+    for s in range(n_shards):
+        oracle_shard_step(rc, inp, s, n_shards)
+    dt = time.perf_counter() - t0
+    return {"value": round(1.0 / dt, 5), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"one full block of {rc.name} (all {rc.shape.block} slots, whole vocabulary) through the "
+                      f"numpy float64 oracle: {dt:.1f} s; OpenBLAS threads = host cores"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    rc, inp = make_workload(args.config)
+    # calibrate the per-step sample: a vocabulary shard sized so warm-up + timed steps stay
+    # within a few minutes
+    n_shards = 64
+    t0 = time.perf_counter()
+    oracle_shard_step(rc, inp, 0, n_shards)
+    t_one = time.perf_counter() - t0
+    budget = 150.0
+    while n_shards > 1 and t_one * 2 * (args.steps + args.warmup) < budget:
+        n_shards //= 2
+        t_one *= 2
+    for i in range(args.warmup):
+        oracle_shard_step(rc, inp, i % n_shards, n_shards)
+    times = []
+    for i in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_shard_step(rc, inp, i % n_shards, n_shards)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = args.steps / n_shards / total
+    sample = (f"each step: the oracle's whole tail on 1/{n_shards} of the vocabulary "
+              f"({rc.shape.vocab // n_shards} tokens) for all {rc.shape.block} slots of {rc.name}; "
+              f"blocks counted as steps/{n_shards}")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded Philox inputs, random weights)",
+            "config": {"workload": rc.name, "batch": rc.shape.batch, "block": rc.shape.block},
+            "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    if args.kernel:
+        run_kernel_case(args)
+        return
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    import torch
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    line, rc, inp = run_ours(args, rank, world, local_rank)
+    if rank == 0 and world == 1 and not args.no_extra:
+        line["cpu_baseline"] = cpu_baseline(rc, inp)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

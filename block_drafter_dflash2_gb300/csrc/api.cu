@@ -1,0 +1,358 @@
+// C ABI of the DFlash2 draft tail: host-side validation, workspace layout, TMA tensor-map
+// encoding and the launch sequence. No allocation, no synchronisation (except
+// dflash2_read_device_error).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "../../include/dflash2.h"
+#include "kernels.h"
+
+namespace {
+
+using df::TcGemmArgs;
+
+constexpr int kMaxDevices = 64;
+
+int g_sm_count[kMaxDevices];
+std::once_flag g_encode_once;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  if (g_sm_count[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    g_sm_count[dev] = n;
+  }
+  return g_sm_count[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode;
+}
+
+// Row-major bf16 matrix [rows, inner] as a 2-D TMA map with a (64 x box_rows) box,
+// 128-byte swizzle, zero fill out of bounds.
+bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  auto enc = encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Plan {
+  int B, T, H, V, K, R, NL, P, M;
+  bool bf16;
+  size_t esz;
+  int n_rc;
+  int lm_parts;
+  int conv_parts;
+  bool raw, greedy;
+};
+
+dflash2_status_t make_plan(const dflash2_shape_t* s, Plan& p) {
+  if (!s) return DFLASH2_ERR_INVALID_ARGUMENT;
+  if (s->batch < 1 || s->block < 1 || s->hidden < 1 || s->vocab < 1 || s->top_k < 1 || s->rank < 1 ||
+      s->conv_layers < 0)
+    return DFLASH2_ERR_INVALID_ARGUMENT;
+  if (s->dtype != DFLASH2_BF16 && s->dtype != DFLASH2_FP32) return DFLASH2_ERR_INVALID_ARGUMENT;
+  if (s->flags & ~(uint32_t)(DFLASH2_CONV_TAPS_RAW | DFLASH2_WALK_GREEDY)) return DFLASH2_ERR_INVALID_ARGUMENT;
+  if (s->hidden % 64 != 0 || s->conv_group_size != 16 || s->conv_kernel_size != 2 || s->top_k > 16 ||
+      s->top_k > s->vocab || s->rank % 16 != 0 || s->rank > 1024 || s->block > 32 || s->conv_layers > 16)
+    return DFLASH2_ERR_UNSUPPORTED;
+  const int64_t M = (int64_t)s->batch * s->block;
+  if (M > (1 << 20) || (int64_t)s->hidden * s->vocab > (int64_t)1 << 40) return DFLASH2_ERR_UNSUPPORTED;
+  p.B = s->batch;
+  p.T = s->block;
+  p.H = s->hidden;
+  p.V = s->vocab;
+  p.K = s->top_k;
+  p.R = s->rank;
+  p.NL = s->conv_layers;
+  p.P = 2 * s->hidden / 16;
+  p.M = (int)M;
+  p.bf16 = s->dtype == DFLASH2_BF16;
+  p.esz = p.bf16 ? 2 : 4;
+  p.raw = (s->flags & DFLASH2_CONV_TAPS_RAW) != 0;
+  p.greedy = (s->flags & DFLASH2_WALK_GREEDY) != 0;
+  if (!p.bf16 && (p.M > 64 || p.H > 4096)) return DFLASH2_ERR_UNSUPPORTED;
+  const int sms = sm_count();
+  if (sms <= 0) return DFLASH2_ERR_CUDA;
+  const int v_units = (p.V + 15) / 16;
+  const int p_units = (p.P + 15) / 16;
+  if (p.bf16) {
+    p.n_rc = (p.M + 127) / 128;
+    const int per = sms / p.n_rc > 0 ? sms / p.n_rc : 1;
+    p.lm_parts = per < v_units ? per : v_units;
+    p.conv_parts = per < p_units ? per : p_units;
+  } else {
+    p.n_rc = 1;
+    p.lm_parts = sms < v_units ? sms : v_units;
+    p.conv_parts = 0;
+  }
+  if (p.lm_parts > 1024) p.lm_parts = 1024;
+  return DFLASH2_OK;
+}
+
+size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct Ws {
+  int32_t* err;
+  void* conv0;
+  void* conv1;
+  float* part_val;
+  int32_t* part_id;
+  float* part_ms;
+  int32_t* cand_ids;
+  float* cand_lp;
+  float* lse;
+  size_t total;
+};
+
+Ws carve(const Plan& p, void* base) {
+  Ws w{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    void* q = base ? static_cast<char*>(base) + off : nullptr;
+    off += up256(bytes);
+    return q;
+  };
+  const size_t act = (size_t)p.M * p.H * p.esz;
+  w.err = static_cast<int32_t*>(take(256));
+  w.conv0 = take(act);
+  w.conv1 = take(act);
+  w.part_val = static_cast<float*>(take((size_t)p.lm_parts * p.M * 16 * 4));
+  w.part_id = static_cast<int32_t*>(take((size_t)p.lm_parts * p.M * 16 * 4));
+  w.part_ms = static_cast<float*>(take((size_t)p.lm_parts * p.M * 2 * 4));
+  w.cand_ids = static_cast<int32_t*>(take((size_t)p.M * p.K * 4));
+  w.cand_lp = static_cast<float*>(take((size_t)p.M * p.K * 4));
+  w.lse = static_cast<float*>(take((size_t)p.M * 4));
+  w.total = off;
+  return w;
+}
+
+dflash2_status_t check_ws(const Plan& p, void* ws, size_t ws_bytes, Ws& w) {
+  if (!ws || !aligned16(ws)) return DFLASH2_ERR_INVALID_ARGUMENT;
+  w = carve(p, ws);
+  if (ws_bytes < w.total) return DFLASH2_ERR_WORKSPACE_TOO_SMALL;
+  return DFLASH2_OK;
+}
+
+dflash2_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? DFLASH2_OK : DFLASH2_ERR_CUDA; }
+
+// ---- stages (arguments already validated)
+
+dflash2_status_t run_conv(const Plan& p, const void* x, const void* conv_w, void* y, const Ws& w,
+                          cudaStream_t s) {
+  const size_t act = (size_t)p.M * p.H * p.esz;
+  if (p.NL == 0) return cuda_status(cudaMemcpyAsync(y, x, act, cudaMemcpyDeviceToDevice, s));
+  const void* cur = x;
+  for (int l = 0; l < p.NL; ++l) {
+    void* out = (l == p.NL - 1) ? y : ((l % 2 == 0) ? w.conv0 : w.conv1);
+    const char* wl = static_cast<const char*>(conv_w) + (size_t)l * p.P * p.H * p.esz;
+    if (p.bf16) {
+      CUtensorMap ma, mb128, mb16;
+      if (!encode_bf16_2d(&ma, cur, p.H, p.M, 128) || !encode_bf16_2d(&mb128, wl, p.H, p.P, 128) ||
+          !encode_bf16_2d(&mb16, wl, p.H, p.P, 16))
+        return DFLASH2_ERR_CUDA;
+      TcGemmArgs a{p.M, p.H, p.P, p.n_rc, p.conv_parts, w.err};
+      if (df::launch_conv_layer_bf16(ma, mb128, mb16, a, cur, out, p.T, p.raw ? 1 : 0, s) != cudaSuccess)
+        return DFLASH2_ERR_CUDA;
+    } else {
+      if (df::launch_conv_layer_f32(static_cast<const float*>(cur), reinterpret_cast<const float*>(wl),
+                                    static_cast<float*>(out), p.M, p.H, p.T, p.raw ? 1 : 0, s) != cudaSuccess)
+        return DFLASH2_ERR_CUDA;
+    }
+    cur = out;
+  }
+  return DFLASH2_OK;
+}
+
+dflash2_status_t run_partials(const Plan& p, const void* rows, const void* lm_head, const Ws& w, cudaStream_t s) {
+  TcGemmArgs a{p.M, p.H, p.V, p.n_rc, p.lm_parts, w.err};
+  if (p.bf16) {
+    CUtensorMap ma, mb128, mb16;
+    if (!encode_bf16_2d(&ma, rows, p.H, p.M, 128) || !encode_bf16_2d(&mb128, lm_head, p.H, p.V, 128) ||
+        !encode_bf16_2d(&mb16, lm_head, p.H, p.V, 16))
+      return DFLASH2_ERR_CUDA;
+    if (df::launch_lmhead_topk_bf16(ma, mb128, mb16, a, w.part_val, w.part_id, w.part_ms, s) != cudaSuccess)
+      return DFLASH2_ERR_CUDA;
+  } else {
+    if (df::launch_lmhead_topk_f32(static_cast<const float*>(rows), static_cast<const float*>(lm_head), a,
+                                   w.part_val, w.part_id, w.part_ms, s) != cudaSuccess)
+      return DFLASH2_ERR_CUDA;
+  }
+  return DFLASH2_OK;
+}
+
+dflash2_status_t run_merge(const Plan& p, int32_t* ids, float* lp, float* lse, const Ws& w, cudaStream_t s) {
+  return cuda_status(
+      df::launch_topk_merge(w.part_val, w.part_id, w.part_ms, p.lm_parts, p.M, p.K, ids, lp, lse ? lse : w.lse, s));
+}
+
+dflash2_status_t run_topk(const Plan& p, const void* rows, const void* lm_head, int32_t* ids, float* lp,
+                          float* lse, const Ws& w, cudaStream_t s) {
+  dflash2_status_t st = run_partials(p, rows, lm_head, w, s);
+  if (st != DFLASH2_OK) return st;
+  return run_merge(p, ids, lp, lse, w, s);
+}
+
+dflash2_status_t run_walk(const Plan& p, const int32_t* anchor, const int32_t* ids, const float* lp,
+                          const void* U, const void* V, int32_t* path_ids, int32_t* path_idx, float* score,
+                          const Ws& w, cudaStream_t s) {
+  return cuda_status(df::launch_transition_walk(p.bf16, anchor, ids, lp, U, V, p.B, p.T, p.K, p.R, p.V,
+                                                p.greedy ? 1 : 0, path_ids, path_idx, score, w.err, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t dflash2_workspace_size(const dflash2_shape_t* shape) {
+  Plan p;
+  if (make_plan(shape, p) != DFLASH2_OK) return 0;
+  return carve(p, nullptr).total;
+}
+
+dflash2_status_t dflash2_conv(const dflash2_shape_t* shape, const void* x, const void* conv_w, void* y, void* ws,
+                              size_t ws_bytes, void* stream) {
+  Plan p;
+  dflash2_status_t st = make_plan(shape, p);
+  if (st != DFLASH2_OK) return st;
+  if (!x || !y || (p.NL > 0 && !conv_w) || x == y) return DFLASH2_ERR_INVALID_ARGUMENT;
+  if (!aligned16(x) || !aligned16(y) || (conv_w && !aligned16(conv_w))) return DFLASH2_ERR_INVALID_ARGUMENT;
+  Ws w;
+  if ((st = check_ws(p, ws, ws_bytes, w)) != DFLASH2_OK) return st;
+  return run_conv(p, x, conv_w, y, w, static_cast<cudaStream_t>(stream));
+}
+
+dflash2_status_t dflash2_select_topk(const dflash2_shape_t* shape, const void* rows, const void* lm_head,
+                                     int32_t* cand_ids, float* cand_lp, float* lse, void* ws, size_t ws_bytes,
+                                     void* stream) {
+  Plan p;
+  dflash2_status_t st = make_plan(shape, p);
+  if (st != DFLASH2_OK) return st;
+  if (!rows || !lm_head || !cand_ids || !cand_lp) return DFLASH2_ERR_INVALID_ARGUMENT;
+  if (!aligned16(rows) || !aligned16(lm_head)) return DFLASH2_ERR_INVALID_ARGUMENT;
+  Ws w;
+  if ((st = check_ws(p, ws, ws_bytes, w)) != DFLASH2_OK) return st;
+  return run_topk(p, rows, lm_head, cand_ids, cand_lp, lse, w, static_cast<cudaStream_t>(stream));
+}
+
+dflash2_status_t dflash2_lmhead_partials(const dflash2_shape_t* shape, const void* rows, const void* lm_head,
+                                         void* ws, size_t ws_bytes, void* stream) {
+  Plan p;
+  dflash2_status_t st = make_plan(shape, p);
+  if (st != DFLASH2_OK) return st;
+  if (!rows || !lm_head) return DFLASH2_ERR_INVALID_ARGUMENT;
+  if (!aligned16(rows) || !aligned16(lm_head)) return DFLASH2_ERR_INVALID_ARGUMENT;
+  Ws w;
+  if ((st = check_ws(p, ws, ws_bytes, w)) != DFLASH2_OK) return st;
+  return run_partials(p, rows, lm_head, w, static_cast<cudaStream_t>(stream));
+}
+
+dflash2_status_t dflash2_merge_partials(const dflash2_shape_t* shape, int32_t* cand_ids, float* cand_lp, float* lse,
+                                        void* ws, size_t ws_bytes, void* stream) {
+  Plan p;
+  dflash2_status_t st = make_plan(shape, p);
+  if (st != DFLASH2_OK) return st;
+  if (!cand_ids || !cand_lp) return DFLASH2_ERR_INVALID_ARGUMENT;
+  Ws w;
+  if ((st = check_ws(p, ws, ws_bytes, w)) != DFLASH2_OK) return st;
+  return run_merge(p, cand_ids, cand_lp, lse, w, static_cast<cudaStream_t>(stream));
+}
+
+dflash2_status_t dflash2_viterbi(const dflash2_shape_t* shape, const int32_t* anchor, const int32_t* cand_ids,
+                                 const float* cand_lp, const void* U, const void* V, int32_t* path_ids,
+                                 int32_t* path_idx, float* score, void* ws, size_t ws_bytes, void* stream) {
+  Plan p;
+  dflash2_status_t st = make_plan(shape, p);
+  if (st != DFLASH2_OK) return st;
+  if (!anchor || !cand_ids || !cand_lp || !U || !V || !path_ids || !path_idx || !score)
+    return DFLASH2_ERR_INVALID_ARGUMENT;
+  if (!aligned16(U) || !aligned16(V)) return DFLASH2_ERR_INVALID_ARGUMENT;
+  Ws w;
+  if ((st = check_ws(p, ws, ws_bytes, w)) != DFLASH2_OK) return st;
+  return run_walk(p, anchor, cand_ids, cand_lp, U, V, path_ids, path_idx, score, w,
+                  static_cast<cudaStream_t>(stream));
+}
+
+dflash2_status_t dflash2_draft_tail(const dflash2_shape_t* shape, const void* hidden, const void* lm_head,
+                                    const void* U, const void* V, const void* conv_w, const int32_t* anchor,
+                                    int32_t* path_ids, int32_t* path_idx, float* score, int32_t* cand_ids,
+                                    float* cand_lp, float* lse, void* ws, size_t ws_bytes, void* stream) {
+  Plan p;
+  dflash2_status_t st = make_plan(shape, p);
+  if (st != DFLASH2_OK) return st;
+  if (!hidden || !lm_head || !U || !V || (p.NL > 0 && !conv_w) || !anchor || !path_ids || !path_idx || !score)
+    return DFLASH2_ERR_INVALID_ARGUMENT;
+  if (!aligned16(hidden) || !aligned16(lm_head) || !aligned16(U) || !aligned16(V) ||
+      (conv_w && !aligned16(conv_w)))
+    return DFLASH2_ERR_INVALID_ARGUMENT;
+  Ws w;
+  if ((st = check_ws(p, ws, ws_bytes, w)) != DFLASH2_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // z: the last conv layer's output lands in conv0/conv1 (never the caller's hidden)
+  const void* z = hidden;
+  if (p.NL > 0) {
+    // Layers l < NL-1 write conv0 (even l) / conv1 (odd l); the last layer writes the buffer that
+    // layer NL-2 did not write, so no layer reads and writes the same buffer.
+    void* zbuf = (p.NL % 2 == 1) ? w.conv0 : w.conv1;
+    if ((st = run_conv(p, hidden, conv_w, zbuf, w, s)) != DFLASH2_OK) return st;
+    z = zbuf;
+  }
+  int32_t* ids = cand_ids ? cand_ids : w.cand_ids;
+  float* lp = cand_lp ? cand_lp : w.cand_lp;
+  if ((st = run_topk(p, z, lm_head, ids, lp, lse, w, s)) != DFLASH2_OK) return st;
+  return run_walk(p, anchor, ids, lp, U, V, path_ids, path_idx, score, w, s);
+}
+
+dflash2_status_t dflash2_read_device_error(void* ws, void* stream, int32_t* code_out) {
+  if (!ws || !code_out) return DFLASH2_ERR_INVALID_ARGUMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t host = 0;
+  if (cudaMemcpyAsync(&host, ws, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return DFLASH2_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DFLASH2_ERR_CUDA;
+  *code_out = host;
+  if (host != 0) {
+    if (cudaMemsetAsync(ws, 0, sizeof(int32_t), s) != cudaSuccess) return DFLASH2_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return DFLASH2_ERR_CUDA;
+  }
+  return DFLASH2_OK;
+}
+
+const char* dflash2_status_string(dflash2_status_t status) {
+  switch (status) {
+    case DFLASH2_OK: return "ok";
+    case DFLASH2_ERR_INVALID_ARGUMENT: return "invalid argument (null, misaligned or bad size)";
+    case DFLASH2_ERR_UNSUPPORTED: return "shape outside the supported set";
+    case DFLASH2_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case DFLASH2_ERR_CUDA: return "CUDA runtime or launch error";
+    case DFLASH2_ERR_DEVICE: return "device error word set";
+  }
+  return "unknown status";
+}
+
+int32_t dflash2_version(void) { return 100; }
+
+}  // extern "C"

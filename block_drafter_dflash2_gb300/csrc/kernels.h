@@ -1,0 +1,38 @@
+// Internal launchers shared by the C-ABI layer (api.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tc_gemm_args.h"
+
+namespace df {
+
+// tcgen05 GEMM + top-K/lse partials (bf16). grid = n_rc * parts.
+cudaError_t launch_lmhead_topk_bf16(const CUtensorMap& a, const CUtensorMap& b128, const CUtensorMap& b16,
+                                    const TcGemmArgs& args, float* part_val, int32_t* part_id,
+                                    float* part_ms, cudaStream_t s);
+
+// tcgen05 GEMM + conv-layer epilogue (bf16): y = mix(x) with taps = x * W^T.
+cudaError_t launch_conv_layer_bf16(const CUtensorMap& a, const CUtensorMap& b128, const CUtensorMap& b16,
+                                   const TcGemmArgs& args, const void* x, void* y, int T, int raw,
+                                   cudaStream_t s);
+
+// fp32 instantiations (small sizes).
+cudaError_t launch_conv_layer_f32(const float* x, const float* w, float* y, int M, int H, int T, int raw,
+                                  cudaStream_t s);
+cudaError_t launch_lmhead_topk_f32(const float* z, const float* w, const TcGemmArgs& args, float* part_val,
+                                   int32_t* part_id, float* part_ms, cudaStream_t s);
+
+// Merge of the per-partition top-16 lists and (max, sum) pairs -> top-K, log-probs, lse.
+cudaError_t launch_topk_merge(const float* part_val, const int32_t* part_id, const float* part_ms, int parts,
+                              int M, int K, int32_t* cand_ids, float* cand_lp, float* lse, cudaStream_t s);
+
+// Transition tiles + Viterbi / greedy walk, one CTA per sequence.
+cudaError_t launch_transition_walk(bool bf16, const int32_t* anchor, const int32_t* cand_ids,
+                                   const float* cand_lp, const void* U, const void* V, int B, int T, int K,
+                                   int R, int vocab, int greedy, int32_t* path_ids, int32_t* path_idx,
+                                   float* score, int32_t* err, cudaStream_t s);
+
+}  // namespace df

@@ -1,0 +1,368 @@
+// Persistent tcgen05 GEMM with a fused epilogue: D = A * B^T, A = rows [M, K] bf16, B = [N, K] bf16.
+//
+// Layout: rows sit on the MMA M dimension (128 TMEM lanes), columns on N. One epilogue
+// thread owns one row and sees that row's N values of a tile in its registers, so a per-row
+// reduction (top-K, log-sum-exp, the conv's per-group tap softmax) is sequential per thread
+// with no cross-thread exchange.
+//
+// Work split: CTA c takes row chunk c % n_rc (128 rows) and column partition c / n_rc of
+// `parts` contiguous ranges (in units of 16 columns, balanced to one unit). A range is walked
+// in tiles of up to 128 columns; the last tile of a range is narrower (16..112 columns) and
+// is fetched in 16-row TMA boxes, so no column outside the range is ever loaded.
+//
+// Roles (192 threads): warp 0 = TMA producer (one thread), warp 1 = MMA issuer (one thread)
+// and TMEM owner, warps 2..5 = epilogue (thread = TMEM lane = row). Shared memory holds a
+// kStages-deep ring of (A 128x64, B 128x64) bf16 tiles in the 128-byte swizzled K-major
+// layout; TMEM holds two 128-column fp32 accumulators so the epilogue of tile t overlaps
+// the MMAs of tile t+1.
+#pragma once
+
+#include "ptx.cuh"
+#include "tc_gemm_args.h"
+
+namespace df {
+
+constexpr int kBK = 64;   // K per stage: one 128-byte swizzle row of bf16
+constexpr int kBM = 128;  // rows per tile (MMA M)
+constexpr int kBN = 128;  // widest tile (MMA N)
+constexpr int kStages = 6;
+constexpr int kTileABytes = kBM * kBK * 2;
+constexpr int kTileBBytes = kBN * kBK * 2;
+constexpr int kStageBytes = kTileABytes + kTileBBytes;
+constexpr int kGemmThreads = 192;
+constexpr int kTmemCols = 2 * kBN;
+constexpr int kGemmSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+
+struct TileRange {
+  int u0, u1;      // unit range [u0, u1) of 16 columns
+  int col_end;     // min(u1 * 16, n_total)
+  int num_tiles;
+};
+
+DF_DEV TileRange tile_range(const TcGemmArgs& a, int part) {
+  TileRange r;
+  const int units = (a.n_total + 15) / 16;
+  r.u0 = (int)((int64_t)part * units / a.parts);
+  r.u1 = (int)((int64_t)(part + 1) * units / a.parts);
+  r.col_end = min(r.u1 * 16, a.n_total);
+  r.num_tiles = (r.u1 - r.u0 + 7) / 8;
+  return r;
+}
+
+template <class Epi>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b128,
+                   const __grid_constant__ CUtensorMap map_b16, const TcGemmArgs args,
+                   const typename Epi::Params ep) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* tfull = empty + kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int rc = blockIdx.x % args.n_rc;
+  const int part = blockIdx.x / args.n_rc;
+  if (part >= args.parts) return;  // whole CTA idle (uniform)
+  const TileRange tr = tile_range(args, part);
+  const int kblocks = args.K / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 32 * 0) {
+    tma_prefetch_desc(&map_a);
+    tma_prefetch_desc(&map_b128);
+    tma_prefetch_desc(&map_b16);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      const uint64_t pol_a = l2_policy_evict_last();   // row tiles are re-read for every column tile
+      const uint64_t pol_b = l2_policy_evict_first();  // column tiles (weights) stream through once
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, issued_phase = 0;  // per-stage bits: ever issued / parity of last issue
+      bool ok = true;
+      for (int t = 0; t < tr.num_tiles && ok; ++t) {
+        const int cu0 = tr.u0 + t * 8;
+        const int nu = min(8, tr.u1 - cu0);
+        const int n0 = cu0 * 16;
+        const uint32_t bytes = kTileABytes + nu * 16 * kBK * 2;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, args.err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + stage * kStageBytes;
+          uint8_t* sb = sa + kTileABytes;
+          mbar_arrive_expect_tx(&full[stage], bytes);
+          tma_load_2d(sa, &map_a, &full[stage], kb * kBK, rc * kBM, pol_a);
+          if (nu == 8) {
+            tma_load_2d(sb, &map_b128, &full[stage], kb * kBK, n0, pol_b);
+          } else {
+            for (int j = 0; j < nu; ++j)
+              tma_load_2d(sb + j * 16 * kBK * 2, &map_b16, &full[stage], kb * kBK, n0 + 16 * j, pol_b);
+          }
+          issued |= 1u << stage;
+          issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // Aborted: let every copy still in flight land before the CTA can exit.
+        for (int s = 0; s < kStages; ++s)
+          if (issued & (1u << s)) mbar_wait(&full[s], (issued_phase >> s) & 1u, args.err, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = 0; t < tr.num_tiles && ok; ++t) {
+        const int acc = t & 1;
+        const uint32_t acc_phase = (uint32_t)(t >> 1) & 1u;
+        const int nu = min(8, tr.u1 - (tr.u0 + t * 8));
+        const uint32_t idesc = idesc_bf16_f32(kBM, nu * 16);
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, args.err, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kBN);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&full[stage], phase, args.err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * kStageBytes);
+          const uint64_t da = sdesc_k_sw128(sa);
+          const uint64_t db = sdesc_k_sw128(sa + kTileABytes);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)  // 16 bf16 = 32 B per MMA along K: +2 in 16-B units
+            umma_bf16(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+          umma_commit(&empty[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) umma_commit(&tfull[acc]);
+      }
+      // Make sure no MMA is still running before TMEM is released.
+      umma_commit(drain);
+      mbar_wait(drain, 0, args.err, nullptr);
+    }
+  } else {
+    // ---------------- epilogue: thread = TMEM lane = row of the chunk
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int row = rc * kBM + q * 32 + lane;
+    const bool row_ok = row < args.M;
+    const bool warp_rows = rc * kBM + q * 32 < args.M;
+    typename Epi::State st;
+    Epi::init(st);
+    for (int t = 0; t < tr.num_tiles; ++t) {
+      const int acc = t & 1;
+      const uint32_t acc_phase = (uint32_t)(t >> 1) & 1u;
+      const int n0 = (tr.u0 + t * 8) * 16;
+      const int nt = min(8, tr.u1 - (tr.u0 + t * 8)) * 16;
+      if (!mbar_wait(&tfull[acc], acc_phase, args.err, abort_flag)) break;
+      tc_fence_after();
+      if (warp_rows) {
+        for (int c = 0; c < nt; c += 32) {
+          float v[32];
+          tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kBN + c), v);
+          Epi::consume(st, ep, v, row, row_ok, n0 + c, min(32, nt - c), tr.col_end);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+    }
+    if (!*abort_flag) Epi::finish(st, ep, row, row_ok, part);
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Epilogue 1: running top-16 (logit desc, id asc) and online log-sum-exp per row.
+// Each thread sees its row's columns in increasing id order, so inserting only values
+// strictly above the current 16th keeps equal logits in id order.
+// ---------------------------------------------------------------------------
+constexpr int kKeep = 16;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct EpiTopK {
+  struct Params {
+    float* part_val;    // [parts][M][16]
+    int32_t* part_id;   // [parts][M][16]
+    float* part_ms;     // [parts][M][2]  (running max, sum of exp(l - max))
+    int M;
+  };
+  struct State {
+    float m, s;
+    float v[kKeep];
+    int32_t id[kKeep];
+  };
+  static DF_DEV void init(State& st) {
+    st.m = -INFINITY;
+    st.s = 0.f;
+#pragma unroll
+    for (int i = 0; i < kKeep; ++i) {
+      st.v[i] = -INFINITY;
+      st.id[i] = 0x7fffffff;
+    }
+  }
+  static DF_DEV void insert(State& st, float x, int32_t id) {
+    // x > st.v[15]: positions below the insertion point shift down by one.
+#pragma unroll
+    for (int i = kKeep - 1; i >= 1; --i) {
+      const bool down = x > st.v[i - 1];
+      const bool here = x > st.v[i];
+      st.v[i] = down ? st.v[i - 1] : (here ? x : st.v[i]);
+      st.id[i] = down ? st.id[i - 1] : (here ? id : st.id[i]);
+    }
+    if (x > st.v[0]) {
+      st.v[0] = x;
+      st.id[0] = id;
+    }
+  }
+  static DF_DEV void consume(State& st, const Params&, const float (&v)[32], int, bool row_ok, int col0,
+                             int ncols, int col_end) {
+    if (!row_ok) return;
+    const int nvalid = min(ncols, col_end - col0);
+    float cm = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < nvalid) cm = fmaxf(cm, v[i]);
+    if (cm == -INFINITY) return;
+    if (cm > st.m) {
+      st.s *= ex2_approx((st.m - cm) * kLog2e);
+      st.m = cm;
+    }
+    const float mb = st.m * kLog2e;
+    float acc = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < nvalid) acc += ex2_approx(fmaf(v[i], kLog2e, -mb));
+    st.s += acc;
+    if (cm > st.v[kKeep - 1]) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i < nvalid && v[i] > st.v[kKeep - 1]) insert(st, v[i], col0 + i);
+    }
+  }
+  static DF_DEV void finish(const State& st, const Params& p, int row, bool row_ok, int part) {
+    if (!row_ok) return;
+    const size_t base = ((size_t)part * p.M + row);
+    float4* pv = reinterpret_cast<float4*>(p.part_val + base * kKeep);
+    int4* pi = reinterpret_cast<int4*>(p.part_id + base * kKeep);
+#pragma unroll
+    for (int i = 0; i < kKeep / 4; ++i) {
+      pv[i] = make_float4(st.v[4 * i], st.v[4 * i + 1], st.v[4 * i + 2], st.v[4 * i + 3]);
+      pi[i] = make_int4(st.id[4 * i], st.id[4 * i + 1], st.id[4 * i + 2], st.id[4 * i + 3]);
+    }
+    reinterpret_cast<float2*>(p.part_ms)[base] = make_float2(st.m, st.s);
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Epilogue 2: one conv layer. Columns are the projection outputs (taps); column pair
+// (2g, 2g+1) gives group g's taps for this row's position t. The epilogue normalises them
+// (softmax over the pair, unless raw) and writes y[t, c] = a * x[t-1, c] + b * x[t, c]
+// for the group's 16 channels, rounded to bf16, with x[-1] = 0 at each block start.
+// ---------------------------------------------------------------------------
+struct EpiConv {
+  struct Params {
+    const __nv_bfloat16* x;  // [M, H] layer input
+    __nv_bfloat16* y;        // [M, H] layer output
+    int M, H, T;
+    int raw;                 // 1: taps unnormalised
+  };
+  struct State {};
+  static DF_DEV void init(State&) {}
+  static DF_DEV void consume(State&, const Params& p, const float (&v)[32], int row, bool row_ok, int col0,
+                             int ncols, int col_end) {
+    if (!row_ok) return;
+    const bool has_prev = (row % p.T) != 0;
+    const __nv_bfloat16* xr = p.x + (size_t)row * p.H;
+    const __nv_bfloat16* xp = xr - p.H;
+    __nv_bfloat16* yr = p.y + (size_t)row * p.H;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int tap = col0 + 2 * i;
+      if (2 * i < ncols && tap < col_end) {
+        float a, b;
+        const float p0 = v[2 * i], p1 = v[2 * i + 1];
+        if (p.raw) {
+          a = p0;
+          b = p1;
+        } else {
+          const float mx = fmaxf(p0, p1);
+          const float e0 = expf(p0 - mx), e1 = expf(p1 - mx);
+          const float inv = 1.f / (e0 + e1);
+          a = e0 * inv;
+          b = e1 * inv;
+        }
+        const int c0 = (tap >> 1) * 16;
+        const uint4* cur = reinterpret_cast<const uint4*>(xr + c0);
+        uint4 cv[2] = {cur[0], cur[1]};
+        uint4 pv[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+        if (has_prev) {
+          const uint4* prv = reinterpret_cast<const uint4*>(xp + c0);
+          pv[0] = prv[0];
+          pv[1] = prv[1];
+        }
+        uint4 out[2];
+        const __nv_bfloat162* c2 = reinterpret_cast<const __nv_bfloat162*>(cv);
+        const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(pv);
+        __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(out);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float2 cf = __bfloat1622float2(c2[k]);
+          const float2 pf = __bfloat1622float2(p2[k]);
+          const float y0 = fmaf(a, pf.x, b * cf.x);
+          const float y1 = fmaf(a, pf.y, b * cf.y);
+          o2[k] = __floats2bfloat162_rn(y0, y1);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(yr + c0);
+        dst[0] = out[0];
+        dst[1] = out[1];
+      }
+    }
+  }
+  static DF_DEV void finish(const State&, const Params&, int, bool, int) {}
+};
+
+}  // namespace df

@@ -1,0 +1,263 @@
+// Transition tiles and the walk from the anchor, one CTA (8 warps) per sequence.
+//
+// For slot boundary t the previous candidates are the anchor (t = 0, repeated K times) or
+// slot t-1's candidates; the current ones are slot t's. Warp t % 8 gathers the 16 U-rows
+// (previous) and 16 V-rows (current) with 128-bit loads into padded shared memory, R/16
+// k-steps at a time in chunks of up to 128 columns, and forms the 16x16 tile
+// tau_t(i, j) = <U[prev_i], V[cur_j]> with mma.sync m16n8k16 (bf16 in, fp32 accumulate).
+// Warp 0 then runs the recursion over the tiles: lane j holds delta(j); each step takes,
+// for every j, the max over i of delta(i) + tau(i, j) with the lowest i on ties, adds
+// lp_t(j), and keeps the back-pointer; a shuffle arg-max (lowest index on ties) picks the
+// final state and lane 0 reads the path back.
+#include <cuda_bf16.h>
+
+#include "../../include/dflash2.h"
+#include "kernels.h"
+
+namespace df {
+
+namespace {
+constexpr int kWarps = 8;
+constexpr int kKP = 16;         // candidate slots per tile (K padded to 16)
+constexpr int kRChunk = 128;    // embedding columns staged per pass
+constexpr int kRowPad = kRChunk + 8;  // bf16 per staged row: 272 B, keeps ldmatrix conflict-free
+constexpr int kMaxT = 32;
+
+struct SmemWalk {
+  int32_t ids[kMaxT][kKP];
+  float lp[kMaxT][kKP];
+  float tau[kMaxT][kKP][kKP];
+  int8_t bp[kMaxT][kKP];
+  int32_t anchor;
+};
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ int32_t clamp_id(int32_t id, int vocab, int32_t* err, int bit) {
+  if (id < 0 || id >= vocab) {
+    if (err) atomicOr(err, bit);
+    return id < 0 ? 0 : vocab - 1;
+  }
+  return id;
+}
+
+// tau tile for one boundary, bf16 embeddings, on one warp.
+__device__ void tile_bf16(const __nv_bfloat16* __restrict__ U, const __nv_bfloat16* __restrict__ V, int R,
+                          const int32_t* prev, const int32_t* cur, __nv_bfloat16* stA, __nv_bfloat16* stB,
+                          float (&tau)[kKP][kKP]) {
+  const int lane = threadIdx.x & 31;
+  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  for (int r0 = 0; r0 < R; r0 += kRChunk) {
+    const int rc = min(kRChunk, R - r0);  // multiple of 16
+    const int vec_per_row = rc / 8;       // 16-byte vectors per staged row
+    __syncwarp();
+    for (int v = lane; v < kKP * vec_per_row; v += 32) {
+      const int row = v / vec_per_row, cv = v % vec_per_row;
+      const uint4 a = *reinterpret_cast<const uint4*>(U + (size_t)prev[row] * R + r0 + cv * 8);
+      const uint4 b = *reinterpret_cast<const uint4*>(V + (size_t)cur[row] * R + r0 + cv * 8);
+      *reinterpret_cast<uint4*>(stA + row * kRowPad + cv * 8) = a;
+      *reinterpret_cast<uint4*>(stB + row * kRowPad + cv * 8) = b;
+    }
+    __syncwarp();
+    for (int k0 = 0; k0 < rc; k0 += 16) {
+      uint32_t a[4], b[4];
+      {
+        const int r = (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int c = k0 + (lane >> 4) * 8;
+        ldmatrix_x4(static_cast<uint32_t>(__cvta_generic_to_shared(stA + r * kRowPad + c)), a[0], a[1], a[2], a[3]);
+      }
+      {
+        const int n = (lane & 7) + (lane >> 4) * 8;
+        const int c = k0 + ((lane >> 3) & 1) * 8;
+        ldmatrix_x4(static_cast<uint32_t>(__cvta_generic_to_shared(stB + n * kRowPad + c)), b[0], b[1], b[2], b[3]);
+      }
+      mma_bf16_16816(acc[0], a, b[0], b[1]);
+      mma_bf16_16816(acc[1], a, b[2], b[3]);
+    }
+  }
+  const int g = lane >> 2, c2 = (lane & 3) * 2;
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    tau[g][nt * 8 + c2] = acc[nt][0];
+    tau[g][nt * 8 + c2 + 1] = acc[nt][1];
+    tau[g + 8][nt * 8 + c2] = acc[nt][2];
+    tau[g + 8][nt * 8 + c2 + 1] = acc[nt][3];
+  }
+}
+
+// tau tile for one boundary, fp32 embeddings (small instantiation): 8 entries per lane.
+__device__ void tile_f32(const float* __restrict__ U, const float* __restrict__ V, int R, const int32_t* prev,
+                         const int32_t* cur, float (&tau)[kKP][kKP]) {
+  const int lane = threadIdx.x & 31;
+  for (int e = lane; e < kKP * kKP; e += 32) {
+    const int i = e / kKP, j = e % kKP;
+    const float* u = U + (size_t)prev[i] * R;
+    const float* v = V + (size_t)cur[j] * R;
+    float s = 0.f;
+    for (int r = 0; r < R; ++r) s = fmaf(u[r], v[r], s);
+    tau[i][j] = s;
+  }
+}
+
+template <bool kBf16>
+__global__ void __launch_bounds__(32 * kWarps)
+    transition_walk_kernel(const int32_t* __restrict__ anchor, const int32_t* __restrict__ cand_ids,
+                           const float* __restrict__ cand_lp, const void* __restrict__ Uv,
+                           const void* __restrict__ Vv, int T, int K, int R, int vocab, int greedy,
+                           int32_t* __restrict__ path_ids, int32_t* __restrict__ path_idx, float* __restrict__ score,
+                           int32_t* err) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  SmemWalk& sw = *reinterpret_cast<SmemWalk*>(smem_raw);
+  __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(smem_raw + ((sizeof(SmemWalk) + 127) & ~size_t(127)));
+  const int b = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) sw.anchor = clamp_id(anchor[b], vocab, err, DFLASH2_DEVERR_ANCHOR_RANGE);
+  for (int e = threadIdx.x; e < T * kKP; e += blockDim.x) {
+    const int t = e / kKP, j = e % kKP;
+    if (j < K) {
+      const size_t at = ((size_t)b * T + t) * K + j;
+      sw.ids[t][j] = clamp_id(cand_ids[at], vocab, err, DFLASH2_DEVERR_CANDIDATE_RANGE);
+      sw.lp[t][j] = cand_lp[at];
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < T * kKP; e += blockDim.x) {  // pad slots K..15 with a valid id
+    const int t = e / kKP, j = e % kKP;
+    if (j >= K) {
+      sw.ids[t][j] = sw.ids[t][0];
+      sw.lp[t][j] = -INFINITY;
+    }
+  }
+  __syncthreads();
+
+  for (int t = warp; t < T; t += kWarps) {
+    int32_t prev[kKP];
+    const int32_t* cur = sw.ids[t];
+#pragma unroll
+    for (int i = 0; i < kKP; ++i) prev[i] = (t == 0) ? sw.anchor : sw.ids[t - 1][i];
+    // stage prev ids in shared memory as well (the bf16 path indexes them per lane)
+    __shared__ int32_t prev_s[kWarps][kKP];
+    if (lane < kKP) prev_s[warp][lane] = prev[lane];
+    __syncwarp();
+    if constexpr (kBf16) {
+      __nv_bfloat16* stA = stage + (size_t)warp * 2 * kKP * kRowPad;
+      __nv_bfloat16* stB = stA + kKP * kRowPad;
+      tile_bf16(reinterpret_cast<const __nv_bfloat16*>(Uv), reinterpret_cast<const __nv_bfloat16*>(Vv), R,
+                prev_s[warp], cur, stA, stB, sw.tau[t]);
+    } else {
+      tile_f32(reinterpret_cast<const float*>(Uv), reinterpret_cast<const float*>(Vv), R, prev_s[warp], cur,
+               sw.tau[t]);
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+
+  if (warp != 0) return;
+  const int j = lane;
+  const bool live = j < K;
+  if (!greedy) {
+    // Viterbi in fp32: delta_0 = lp_0 + tau_0(0, j); delta_t = lp_t + max_i (delta_{t-1}(i) + tau_t(i, j)).
+    float delta = live ? sw.lp[0][j] + sw.tau[0][0][j] : -INFINITY;
+    for (int t = 1; t < T; ++t) {
+      float best = 0.f;
+      int arg = 0;
+      for (int i = 0; i < K; ++i) {
+        const float di = __shfl_sync(0xffffffffu, delta, i);
+        if (live) {
+          const float v = di + sw.tau[t][i][j];
+          if (i == 0 || v > best) {
+            best = v;
+            arg = i;
+          }
+        }
+      }
+      if (live) {
+        delta = sw.lp[t][j] + best;
+        sw.bp[t][j] = (int8_t)arg;
+      }
+    }
+    // arg-max over lanes, lowest index on ties
+    float bv = delta;
+    int bj = live ? j : 0x7fffffff;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oj = __shfl_xor_sync(0xffffffffu, bj, o);
+      if (oj < 0x7fffffff && (bj == 0x7fffffff || ov > bv || (ov == bv && oj < bj))) {
+        bv = ov;
+        bj = oj;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      int cj = bj;
+      for (int t = T - 1; t >= 0; --t) {
+        path_idx[(size_t)b * T + t] = cj;
+        path_ids[(size_t)b * T + t] = sw.ids[t][cj];
+        if (t > 0) cj = sw.bp[t][cj];
+      }
+      score[b] = bv;
+    }
+  } else {
+    // Greedy: j_t = argmax_j (lp_t(j) + tau_t(j_{t-1}, j)); the score follows the Viterbi
+    // recursion's order on the chosen path: delta_t = lp_t(j_t) + (delta_{t-1} + tau_t(j_{t-1}, j_t)).
+    if (lane == 0) {
+      float delta = 0.f;
+      int pj = 0;
+      for (int t = 0; t < T; ++t) {
+        int bj = 0;
+        float bv = 0.f;
+        for (int c = 0; c < K; ++c) {
+          const float v = sw.lp[t][c] + sw.tau[t][t == 0 ? 0 : pj][c];
+          if (c == 0 || v > bv) {
+            bv = v;
+            bj = c;
+          }
+        }
+        delta = (t == 0) ? sw.lp[0][bj] + sw.tau[0][0][bj] : sw.lp[t][bj] + (delta + sw.tau[t][pj][bj]);
+        path_idx[(size_t)b * T + t] = bj;
+        path_ids[(size_t)b * T + t] = sw.ids[t][bj];
+        pj = bj;
+      }
+      score[b] = delta;
+    }
+  }
+}
+}  // namespace
+
+cudaError_t launch_transition_walk(bool bf16, const int32_t* anchor, const int32_t* cand_ids,
+                                   const float* cand_lp, const void* U, const void* V, int B, int T, int K,
+                                   int R, int vocab, int greedy, int32_t* path_ids, int32_t* path_idx,
+                                   float* score, int32_t* err, cudaStream_t s) {
+  if (T > kMaxT || K > kKP) return cudaErrorInvalidValue;
+  const size_t base = (sizeof(SmemWalk) + 127) & ~size_t(127);
+  const size_t smem = base + (bf16 ? (size_t)kWarps * 2 * kKP * kRowPad * sizeof(__nv_bfloat16) : 0);
+  cudaError_t e;
+  if (bf16) {
+    e = cudaFuncSetAttribute(transition_walk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    transition_walk_kernel<true><<<B, 32 * kWarps, smem, s>>>(anchor, cand_ids, cand_lp, U, V, T, K, R, vocab,
+                                                               greedy, path_ids, path_idx, score, err);
+  } else {
+    e = cudaFuncSetAttribute(transition_walk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    transition_walk_kernel<false><<<B, 32 * kWarps, smem, s>>>(anchor, cand_ids, cand_lp, U, V, T, K, R, vocab,
+                                                                greedy, path_ids, path_idx, score, err);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace df

@@ -1,0 +1,176 @@
+/*
+ * dflash2.h — C ABI of the DFlash2 draft tail on one NVIDIA GB300 (sm_103a).
+ *
+ * The draft tail runs once per verify step of the DFlash2 parallel drafter:
+ *   1. a grouped dynamic depthwise convolution inside each block, so a proposal
+ *      position sees the positions before it without another backbone pass
+ *      ("vLLM adds DFlash2 ...", section "2つの追加要素" (the two additions);
+ *      shapes from "RTX 4090 ... DFlash2 vs MTP", section 4, dflash_config:
+ *      conv_group_size 16, conv_kernel_size 2);
+ *   2. the LM-head contraction, keeping each slot's top-K tokens and its
+ *      log-sum-exp (selector_top_k 16, same dflash_config; "DFlash 2: keeping
+ *      drafts parallel", section "正しいトークンはすでにそこにあります", Table 1);
+ *   3. pairwise transition scores between adjacent slots' candidates through two
+ *      rank-R token embeddings, and the best path from the verified anchor
+ *      ("DFlash 2: keeping drafts parallel", section "軽量パスセレクター"
+ *      (lightweight path selector); selector_rank 256).
+ *
+ * Conventions for every call:
+ *  - All tensor arguments are caller-owned DEVICE pointers to contiguous,
+ *    row-major memory. bf16 tensors hold IEEE bfloat16 bit patterns.
+ *  - `hidden`, `lm_head`, `U`, `V`, `conv_w`, rows, and the workspace must be
+ *    16-byte aligned (they are read by TMA and 128-bit loads).
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream). Every launch is
+ *    asynchronous on it; no call synchronises except dflash2_read_device_error.
+ *  - The library allocates no memory. Scratch lives in the caller's workspace
+ *    `ws` of `ws_bytes` bytes (query dflash2_workspace_size). Zero the
+ *    workspace once before its first use (it carries the device error word).
+ *    Calls that share a workspace must not overlap in time.
+ *  - Argument errors are detected on the host and returned before any launch.
+ *    A launch failure returns DFLASH2_ERR_CUDA. Data errors found on the device
+ *    (a token id outside [0, vocab), an internal wait that ran out of time) set
+ *    bits in the workspace's error word; the kernel clamps and carries on, and
+ *    dflash2_read_device_error reports and clears them.
+ *  - Supported shapes: hidden % 64 == 0, conv_group_size == 16 (channels per
+ *    group), conv_kernel_size == 2, 1 <= top_k <= 16, top_k <= vocab,
+ *    rank % 16 == 0 and rank <= 1024, 1 <= block <= 32, batch >= 1,
+ *    0 <= conv_layers <= 16. dtype FP32 is a small-size instantiation
+ *    (batch*block <= 64, hidden <= 4096).
+ */
+#ifndef DFLASH2_H
+#define DFLASH2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DFLASH2_OK = 0,
+  DFLASH2_ERR_INVALID_ARGUMENT = 1, /* null pointer, bad size, misaligned pointer */
+  DFLASH2_ERR_UNSUPPORTED = 2,      /* a shape outside the supported set above */
+  DFLASH2_ERR_WORKSPACE_TOO_SMALL = 3,
+  DFLASH2_ERR_CUDA = 4,             /* a CUDA runtime call or launch failed */
+  DFLASH2_ERR_DEVICE = 5            /* the device error word is non-zero */
+} dflash2_status_t;
+
+typedef enum { DFLASH2_BF16 = 0, DFLASH2_FP32 = 1 } dflash2_dtype_t;
+
+/* shape.flags bits */
+enum {
+  DFLASH2_CONV_TAPS_SOFTMAX = 0,      /* default: each group's 2 taps are softmax-normalised */
+  DFLASH2_CONV_TAPS_RAW = 1u << 0,    /* taps used as projected, unnormalised */
+  DFLASH2_WALK_VITERBI = 0,           /* default: exact best path (Viterbi) */
+  DFLASH2_WALK_GREEDY = 1u << 1       /* the pages' greedy walk: best successor at each step */
+};
+
+/* Device error word bits (dflash2_read_device_error). */
+enum {
+  DFLASH2_DEVERR_ANCHOR_RANGE = 1 << 0,    /* an anchor id was outside [0, vocab); clamped */
+  DFLASH2_DEVERR_CANDIDATE_RANGE = 1 << 1, /* a candidate id was outside [0, vocab); clamped */
+  DFLASH2_DEVERR_WAIT_TIMEOUT = 1 << 2     /* an internal pipeline wait ran out of time */
+};
+
+typedef struct {
+  int32_t batch;            /* B: sequences */
+  int32_t block;            /* T: slots per sequence (block_size) */
+  int32_t hidden;           /* H: hidden width (5120 on the pages) */
+  int32_t vocab;            /* V: vocabulary (248,320 on the pages) */
+  int32_t top_k;            /* K: candidates kept per slot (16) */
+  int32_t rank;             /* R: selector embedding width (256) */
+  int32_t conv_group_size;  /* channels per conv group (16) */
+  int32_t conv_kernel_size; /* conv taps (2) */
+  int32_t conv_layers;      /* NL: conv layers chained (5) */
+  int32_t dtype;            /* dflash2_dtype_t of hidden, lm_head, U, V, conv_w */
+  uint32_t flags;           /* DFLASH2_CONV_TAPS_* | DFLASH2_WALK_* */
+} dflash2_shape_t;
+
+/* Bytes of workspace that every call below needs for `shape` on the current
+ * device (one size covers all of them). Returns 0 for an invalid shape. */
+size_t dflash2_workspace_size(const dflash2_shape_t* shape);
+
+/* Grouped dynamic depthwise convolution, all conv_layers chained.
+ *   x      [B, T, H]              input rows (dtype)
+ *   conv_w [NL, 2H/16, H]          per layer, projection row 2g+j gives group g's
+ *                                  tap j; tap 0 weights position t-1, tap 1 position t
+ *   y      [B, T, H]              output (dtype); may not alias x
+ * Per layer, position t and group g: p_j = x[t] . conv_w[l][2g+j];
+ * (a, b) = softmax(p_0, p_1) (or (p_0, p_1) with DFLASH2_CONV_TAPS_RAW);
+ * y[t, c] = a * x[t-1, c] + b * x[t, c] for the 16 channels c of group g, with
+ * x[-1] = 0 inside each sequence's block; each layer's output is rounded to
+ * dtype (bf16: round to nearest even) before the next layer. fp32 accumulation. */
+dflash2_status_t dflash2_conv(const dflash2_shape_t* shape, const void* x, const void* conv_w,
+                              void* y, void* ws, size_t ws_bytes, void* stream);
+
+/* LM-head contraction with per-row top-K and log-sum-exp; the [M, V] logits are
+ * never written to memory.
+ *   rows     [M, H] (M = B*T)      input rows (dtype)
+ *   lm_head  [V, H]                 (dtype)
+ *   cand_ids [M, K] int32           top-K token ids, logit descending, ties to the lower id
+ *   cand_lp  [M, K] fp32            log-softmax of those tokens: logit - lse (fp32)
+ *   lse      [M]    fp32            log sum_v exp(logit[v]); may be NULL
+ * Logits are fp32 dot products of the dtype inputs (fp32 accumulation). */
+dflash2_status_t dflash2_select_topk(const dflash2_shape_t* shape, const void* rows, const void* lm_head,
+                                     int32_t* cand_ids, float* cand_lp, float* lse,
+                                     void* ws, size_t ws_bytes, void* stream);
+
+/* The two stages of dflash2_select_topk, callable on their own (e.g. to time the
+ * contraction, or to merge partials that the caller gathered from several vocab shards).
+ * dflash2_lmhead_partials runs the LM-head contraction with its fused epilogue and leaves,
+ * in the workspace, one partial per (row, column partition): that partition's top-16
+ * (logit desc, id asc) and its (max logit, sum of exp(logit - max)).
+ * dflash2_merge_partials turns the workspace's partials into cand_ids, cand_lp and lse
+ * exactly as dflash2_select_topk does. Both take the same shape and workspace. */
+dflash2_status_t dflash2_lmhead_partials(const dflash2_shape_t* shape, const void* rows, const void* lm_head,
+                                         void* ws, size_t ws_bytes, void* stream);
+dflash2_status_t dflash2_merge_partials(const dflash2_shape_t* shape, int32_t* cand_ids, float* cand_lp,
+                                        float* lse, void* ws, size_t ws_bytes, void* stream);
+
+/* Transition scores and the walk from the anchor.
+ *   anchor   [B] int32              verified token preceding slot 0 of each sequence
+ *   cand_ids [B, T, K] int32, cand_lp [B, T, K] fp32   (as from dflash2_select_topk)
+ *   U, V     [V, R] (dtype)         U embeds the previous token, V the current one
+ *   path_ids [B, T] int32           chosen token per slot
+ *   path_idx [B, T] int32           chosen candidate index per slot
+ *   score    [B] fp32               path score
+ * tau_0(j) = <U[anchor], V[c_{0,j}]>, tau_t(i, j) = <U[c_{t-1,i}], V[c_{t,j}]>;
+ * Viterbi (default): delta_0(j) = lp_0(j) + tau_0(j),
+ * delta_t(j) = lp_t(j) + max_i (delta_{t-1}(i) + tau_t(i, j)), fp32, every
+ * argmax taking the lowest index; score = max_j delta_{T-1}(j).
+ * Greedy (DFLASH2_WALK_GREEDY): j_t = argmax_j (lp_t(j) + tau_t(j_{t-1}, j)),
+ * score accumulated along the path in the same order as the Viterbi recursion. */
+dflash2_status_t dflash2_viterbi(const dflash2_shape_t* shape, const int32_t* anchor,
+                                 const int32_t* cand_ids, const float* cand_lp,
+                                 const void* U, const void* V,
+                                 int32_t* path_ids, int32_t* path_idx, float* score,
+                                 void* ws, size_t ws_bytes, void* stream);
+
+/* The whole tail in one call: conv -> LM head top-K + lse -> transitions + walk.
+ *   hidden [B, T, H], lm_head [V, H], U/V [V, R], conv_w [NL, 2H/16, H], anchor [B]
+ *   path_ids, path_idx [B, T] int32; score [B] fp32
+ *   cand_ids [B, T, K], cand_lp [B, T, K], lse [B, T]: optional copies of the
+ *   intermediate candidates (NULL to skip). */
+dflash2_status_t dflash2_draft_tail(const dflash2_shape_t* shape, const void* hidden, const void* lm_head,
+                                    const void* U, const void* V, const void* conv_w,
+                                    const int32_t* anchor, int32_t* path_ids, int32_t* path_idx,
+                                    float* score, int32_t* cand_ids, float* cand_lp, float* lse,
+                                    void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronises `stream`, returns the workspace's device error word in *code_out
+ * (a DFLASH2_DEVERR_* bit set; 0 = none) and clears it. Returns DFLASH2_OK, or
+ * DFLASH2_ERR_CUDA if the copy failed. */
+dflash2_status_t dflash2_read_device_error(void* ws, void* stream, int32_t* code_out);
+
+/* Static description of a status code. */
+const char* dflash2_status_string(dflash2_status_t status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int32_t dflash2_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DFLASH2_H */

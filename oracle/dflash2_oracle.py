@@ -31,7 +31,7 @@ Readings where the pages are silent (each is a fixed choice, stated where used):
      and no norm before the LM head.
   R5 causal within the block, x[-1] = 0, sequences independent.
   R6 all `block` rows are slots; the anchor is the predecessor of slot 0.
-  R7 per-slot score = log-softmax of the head's logits (spec contract); the
+  R7 per-slot score = log-softmax of the head's logits (this library's contract); the
      pages' raw-logit score gives the same path (per-slot constants cancel).
   R8 the context gate H(h_t) is taken as all-ones.
   R9 the walk is a Viterbi (exact best path); the pages' greedy walk is kept as
@@ -286,17 +286,30 @@ def viterbi_two_best(cand_lp: np.ndarray, tau: np.ndarray):
 
 
 def greedy_walk(cand_lp: np.ndarray, tau: np.ndarray):
-    """The pages' walk: from the anchor, take the best successor at each step
-    (ties to the lower index). Returns (path_idx [B,T], score [B] float64)."""
+    """The pages' walk (R9): from the anchor, take the best successor at each step, in fp32.
+
+    j_0 = argmax_j lp_0(j) + tau_0(0, j); j_t = argmax_j lp_t(j) + tau_t(j_{t-1}, j), lowest j on
+    ties. The score follows the Viterbi recursion's order along the chosen path:
+    d_0 = lp_0(j_0) + tau_0(0, j_0), d_t = lp_t(j_t) + (d_{t-1} + tau_t(j_{t-1}, j_t)).
+    Returns (path_idx [B,T] int32, score [B] float32)."""
     B, T, K = cand_lp.shape
+    lp = cand_lp.astype(np.float32)
+    tt = tau.astype(np.float32)
     path = np.zeros((B, T), dtype=np.int32)
+    score = np.zeros(B, dtype=np.float32)
     for b in range(B):
-        j = int(np.argmax(cand_lp[b, 0].astype(np.float64) + tau[b, 0, 0].astype(np.float64)))
+        v = (lp[b, 0] + tt[b, 0, 0]).astype(np.float32)
+        j = int(np.argmax(v))
+        d = np.float32(v[j])
         path[b, 0] = j
         for t in range(1, T):
-            j = int(np.argmax(cand_lp[b, t].astype(np.float64) + tau[b, t, j].astype(np.float64)))
+            v = (lp[b, t] + tt[b, t, j]).astype(np.float32)
+            jn = int(np.argmax(v))
+            d = np.float32(lp[b, t, jn] + np.float32(d + tt[b, t, j, jn]))
+            j = jn
             path[b, t] = j
-    return path, path_score(cand_lp, tau, path)
+        score[b] = d
+    return path, score
 
 
 def brute_force_best(cand_lp: np.ndarray, tau: np.ndarray):

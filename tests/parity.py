@@ -1,0 +1,227 @@
+"""Parity harness: runs the CUDA library through its C ABI and compares it with the oracle.
+
+Tolerances (from the draft-tail contract): token ids and paths bit-exact except at
+near-ties; lse, candidate log-probs and path scores within 2e-3 absolute; conv outputs
+within 1e-2 relative.
+
+Near-tie rules used here:
+  * top-K: the GPU's k-th candidate may differ from the oracle's k-th only if the two
+    tokens' oracle logits lie within 1e-3 * |max logit| of each other (at the K/K+1
+    boundary this is the set-membership tie; inside the list, an order swap);
+  * paths: the walk is checked exactly on the GPU's own candidates (the oracle Viterbi
+    re-run on them), and against the full oracle path when the sequence had no top-K
+    near-tie; either comparison may differ only when the oracle's best/second-best margin
+    is below 1e-2.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import block_drafter_dflash2_gb300 as df2
+from oracle import core as O
+
+LSE_TOL = 2e-3
+LP_TOL = 2e-3
+SCORE_TOL = 2e-3
+CONV_RTOL = 1e-2
+TIE_REL = 1e-3
+MARGIN = 1e-2
+
+
+def shape_of(sh, greedy=False) -> df2.Shape:
+    return df2.Shape.make(sh.batch, sh.block, sh.hidden, sh.vocab, sh.top_k, sh.rank, sh.layers,
+                          dtype=sh.dtype, raw_taps=(sh.taps == "raw"), greedy=greedy)
+
+
+def dev(a: np.ndarray) -> torch.Tensor:
+    """Upload a numpy array (bf16 bit patterns travel as int16) to cuda:0."""
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    return torch.from_numpy(np.ascontiguousarray(a)).to("cuda:0")
+
+
+def host(t: torch.Tensor, like=None) -> np.ndarray:
+    a = t.cpu().numpy()
+    if a.dtype == np.int16:
+        a = a.view(np.uint16)
+    return a
+
+
+def workspace(shape: df2.Shape) -> torch.Tensor:
+    n = df2.workspace_size(shape)
+    assert n > 0
+    return torch.zeros(n, dtype=torch.uint8, device="cuda:0")
+
+
+def upload_inputs(inp: dict) -> dict:
+    return {k: dev(v) for k, v in inp.items() if v is not None and k in ("hidden", "lm_head", "U", "V", "conv_w", "anchor")}
+
+
+def run_tail(shape: df2.Shape, d: dict, ws=None, stream=None) -> dict:
+    B, T, K = shape.batch, shape.block, shape.top_k
+    o = {
+        "path_ids": torch.empty((B, T), dtype=torch.int32, device="cuda:0"),
+        "path_idx": torch.empty((B, T), dtype=torch.int32, device="cuda:0"),
+        "score": torch.empty((B,), dtype=torch.float32, device="cuda:0"),
+        "cand_ids": torch.empty((B, T, K), dtype=torch.int32, device="cuda:0"),
+        "cand_lp": torch.empty((B, T, K), dtype=torch.float32, device="cuda:0"),
+        "lse": torch.empty((B, T), dtype=torch.float32, device="cuda:0"),
+    }
+    ws = workspace(shape) if ws is None else ws
+    df2.draft_tail(shape, d["hidden"], d["lm_head"], d["U"], d["V"], d["conv_w"], d["anchor"], o["path_ids"],
+                   o["path_idx"], o["score"], ws, cand_ids=o["cand_ids"], cand_lp=o["cand_lp"], lse=o["lse"],
+                   stream=stream)
+    torch.cuda.synchronize()
+    err = df2.read_device_error(ws)
+    out = {k: host(v) for k, v in o.items()}
+    out["device_error"] = err
+    return out
+
+
+def run_conv(shape: df2.Shape, x: torch.Tensor, conv_w: torch.Tensor) -> np.ndarray:
+    y = torch.empty_like(x)
+    ws = workspace(shape)
+    df2.conv(shape, x, conv_w, y, ws)
+    torch.cuda.synchronize()
+    assert df2.read_device_error(ws) == 0
+    return host(y)
+
+
+def run_topk(shape: df2.Shape, rows: torch.Tensor, lm_head: torch.Tensor):
+    M, K = shape.batch * shape.block, shape.top_k
+    ids = torch.empty((M, K), dtype=torch.int32, device="cuda:0")
+    lp = torch.empty((M, K), dtype=torch.float32, device="cuda:0")
+    lse = torch.empty((M,), dtype=torch.float32, device="cuda:0")
+    ws = workspace(shape)
+    df2.select_topk(shape, rows, lm_head, ids, lp, lse, ws)
+    torch.cuda.synchronize()
+    assert df2.read_device_error(ws) == 0
+    return host(ids), host(lp), host(lse)
+
+
+def run_viterbi(shape: df2.Shape, anchor, cand_ids, cand_lp, U, V):
+    B, T = shape.batch, shape.block
+    pid = torch.empty((B, T), dtype=torch.int32, device="cuda:0")
+    pix = torch.empty((B, T), dtype=torch.int32, device="cuda:0")
+    sc = torch.empty((B,), dtype=torch.float32, device="cuda:0")
+    ws = workspace(shape)
+    df2.viterbi(shape, anchor, cand_ids, cand_lp, U, V, pid, pix, sc, ws)
+    torch.cuda.synchronize()
+    err = df2.read_device_error(ws)
+    return host(pid), host(pix), host(sc), err
+
+
+# ------------------------------------------------------------------ comparators
+
+
+def check_conv(z_gpu: np.ndarray, z_ref: np.ndarray, max_ulps=None):
+    """Per element |gpu - ref| <= 1e-2 * max(|ref|, rms of the ref row): "relative" with the
+    denominator floored at the row's scale, because a * x[t-1] + b * x[t] can cancel to near
+    zero while its rounding error stays at the operands' scale. Optionally also bounds the
+    difference in bf16 units in the last place (one layer: at most 1)."""
+    g = O.widen(z_gpu)
+    r = O.widen(z_ref)
+    rms = np.sqrt(np.mean(r * r, axis=-1, keepdims=True))
+    bound = CONV_RTOL * np.maximum(np.abs(r), rms)
+    bad = np.abs(g - r) > bound
+    assert not bad.any(), f"conv: {bad.sum()} of {bad.size} elements outside 1e-2 relative; " \
+                          f"max abs diff {np.abs(g - r).max():.3e}"
+    rep = {"conv_exact_frac": float((g == r).mean()), "conv_max_abs": float(np.abs(g - r).max()),
+           "conv_norm_rel": float(np.linalg.norm(g - r) / max(np.linalg.norm(r), 1e-30))}
+    if max_ulps is not None and z_gpu.dtype == np.uint16:
+        # bf16 bit patterns of same-sign values are ordered like the values
+        gi = z_gpu.astype(np.int32)
+        ri = z_ref.astype(np.int32)
+        same_sign = (gi >> 15) == (ri >> 15)
+        ulps = np.where(same_sign, np.abs(gi - ri), np.abs((gi & 0x7FFF) + (ri & 0x7FFF)))
+        assert ulps.max() <= max_ulps, f"conv: {ulps.max()} ulps apart"
+        rep["conv_max_ulps"] = int(ulps.max())
+    return rep
+
+
+def check_topk(ref: dict, g_ids, g_lp, g_lse, z_rows, lm_head, K):
+    """ref: oracle outputs flattened to rows (cand_ids [M,K], cand_logit, max_logit, lse)."""
+    M = g_ids.shape[0]
+    o_ids = ref["cand_ids"].reshape(M, K)
+    o_val = ref["cand_logit"].reshape(M, K)
+    o_max = ref["max_logit"].reshape(M)
+    o_lse = ref["lse"].reshape(M)
+    lse_err = np.abs(g_lse.reshape(M).astype(np.float64) - o_lse)
+    assert lse_err.max() <= LSE_TOL, f"lse error {lse_err.max():.3e}"
+    tie_rows = []
+    lp_err = 0.0
+    for m in range(M):
+        band = TIE_REL * abs(float(o_max[m]))
+        if np.array_equal(g_ids[m], o_ids[m]):
+            lg = o_val[m]
+        else:
+            assert len(set(g_ids[m].tolist())) == K, f"row {m}: repeated ids {g_ids[m]}"
+            assert np.all((g_ids[m] >= 0) & (g_ids[m] < lm_head.shape[0])), f"row {m}: id out of range"
+            lg = O.logits(z_rows[m:m + 1], lm_head[g_ids[m]])[0]
+            gap = np.abs(lg.astype(np.float64) - o_val[m].astype(np.float64))
+            assert gap.max() <= band, f"row {m}: ids {g_ids[m]} vs {o_ids[m]}, logit gap {gap.max():.3e} > {band:.3e}"
+            tie_rows.append(m)
+        e = np.abs(g_lp[m].astype(np.float64) - (lg.astype(np.float64) - o_lse[m])).max()
+        lp_err = max(lp_err, e)
+    assert lp_err <= LP_TOL, f"cand_lp error {lp_err:.3e}"
+    return {"near_tie_rows": tie_rows, "lse_max_err": float(lse_err.max()), "lp_max_err": float(lp_err)}
+
+
+def check_walk(shape, anchor, U, V, g_ids, g_lp, g_path_idx, g_path_ids, g_score, ref=None, tie_rows=(),
+               greedy=False):
+    """Exact check of the walk on the GPU's own candidates, and (when given) against the full oracle."""
+    B, T, K = shape.batch, shape.block, shape.top_k
+    g_ids = g_ids.reshape(B, T, K)
+    g_lp = g_lp.reshape(B, T, K)
+    tau = O.transitions(anchor, g_ids, U, V)
+    if greedy:
+        o_path, o_score = O.greedy_walk(g_lp, tau)
+        best = second = None
+    else:
+        o_path, o_score = O.viterbi(g_lp, tau)
+        best, second = O.viterbi_two_best(g_lp, tau)
+    stats = {"path_mismatch_small_margin": 0, "path_vs_oracle_mismatch_small_margin": 0}
+    for b in range(B):
+        assert np.array_equal(g_path_ids[b], g_ids[b, np.arange(T), g_path_idx[b]]), f"seq {b}: path ids inconsistent"
+        if not np.array_equal(g_path_idx[b], o_path[b]):
+            margin = (best[b] - second[b]) if best is not None else 0.0
+            assert margin < MARGIN, f"seq {b}: path {g_path_idx[b]} vs {o_path[b]} with margin {margin:.3e}"
+            stats["path_mismatch_small_margin"] += 1
+            assert abs(float(g_score[b]) - float(o_score[b])) <= margin + SCORE_TOL
+        else:
+            assert abs(float(g_score[b]) - float(o_score[b])) <= SCORE_TOL, f"seq {b}: score {g_score[b]} vs {o_score[b]}"
+    if ref is not None:
+        seq_tie = {m // T for m in tie_rows}
+        for b in range(B):
+            if b in seq_tie:
+                continue
+            if not np.array_equal(g_path_idx[b], ref["path_idx"][b]):
+                margin = ref["best"][b] - ref["second"][b]
+                assert margin < MARGIN, f"seq {b}: path vs full oracle differs with margin {margin:.3e}"
+                stats["path_vs_oracle_mismatch_small_margin"] += 1
+            else:
+                assert np.array_equal(g_path_ids[b], ref["path_ids"][b])
+                assert abs(float(g_score[b]) - float(ref["score"][b])) <= SCORE_TOL
+    return stats
+
+
+def check_tail(shape, inp: dict, ref: dict, g: dict, seqs=None) -> dict:
+    """Compare a draft_tail result with the oracle on the listed sequences."""
+    B, T, K, H = shape.batch, shape.block, shape.top_k, shape.hidden
+    seqs = list(range(B)) if seqs is None else list(seqs)
+    assert g["device_error"] == 0, f"device error word {g['device_error']}"
+    sel = np.asarray(seqs)
+    z_rows = ref["z"].reshape(-1, H)
+    rows = (sel[:, None] * T + np.arange(T)[None, :]).reshape(-1)
+    g_ids = g["cand_ids"].reshape(B * T, K)[rows]
+    g_lp = g["cand_lp"].reshape(B * T, K)[rows]
+    g_lse = g["lse"].reshape(B * T)[rows]
+    rep = check_topk(ref, g_ids, g_lp, g_lse, z_rows, inp["lm_head"], K)
+
+    class _S:  # the subset as a shape
+        batch, block, top_k = len(seqs), T, K
+    rep.update(check_walk(_S, np.asarray(inp["anchor"])[sel], inp["U"], inp["V"], g_ids, g_lp,
+                          g["path_idx"][sel], g["path_ids"][sel], g["score"][sel], ref=ref,
+                          tie_rows=rep["near_tie_rows"], greedy=bool(getattr(shape, "greedy", False))))
+    return rep

@@ -1,0 +1,234 @@
+"""GPU parity of every step of the draft tail against the CPU oracle, at sizes the
+oracle finishes in seconds that still span several tiles, ragged tails and the
+edge cases (K < 16, block 1, duplicated anchors and candidates, exact ties, ids out
+of range). Each call goes through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import core as O
+from tests import parity as P
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import block_drafter_dflash2_gb300 as df2
+    assert torch.cuda.is_available()
+    df2.load()
+
+
+def _recipe(base=2, **kw):
+    return synth.scaled_recipe(synth.recipe(base), **kw)
+
+
+# ------------------------------------------------------------------ whole tail, small
+
+CASES = {
+    # several 128-wide vocab tiles per CTA plus a narrow ragged last tile, vocab not a multiple of 16
+    "b3_t8_h512_v70005": dict(batch=3, block=8, hidden=512, vocab=70_005, layers=2),
+    # two row chunks of 128 (160 rows: the second chunk ragged)
+    "b20_t8_h256_v20003": dict(batch=20, block=8, hidden=256, vocab=20_003, layers=1),
+    # eight row chunks, block 16
+    "b64_t16_h256_v8208_r64": dict(batch=64, block=16, hidden=256, vocab=8_208, rank=64, layers=5),
+    # vocab smaller than the number of column partitions, K < 16, block 1
+    "b4_t1_h128_v100_k4": dict(batch=4, block=1, hidden=128, vocab=100, top_k=4, rank=32, layers=3),
+    # no conv layers; rank that is not a multiple of the 128-column staging chunk
+    "b2_t5_h64_v999_r272_nl0": dict(batch=2, block=5, hidden=64, vocab=999, rank=272, layers=0),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_draft_tail_small(name):
+    rc = _recipe(**CASES[name])
+    sh = rc.shape
+    inp = synth.make_inputs(rc)
+    ref = O.draft_tail(inp, sh)
+    g = P.run_tail(P.shape_of(sh), P.upload_inputs(inp))
+    rep = P.check_tail(sh, inp, ref, g)
+    print(name, {k: v for k, v in rep.items() if k != "near_tie_rows"}, "ties", len(rep["near_tie_rows"]))
+
+
+def test_tiny_fp32_workload():
+    rc = synth.recipe(1)
+    sh = rc.shape
+    inp = synth.make_inputs(rc)
+    ref = O.draft_tail(inp, sh)
+    g = P.run_tail(P.shape_of(sh), P.upload_inputs(inp))
+    P.check_tail(sh, inp, ref, g)
+    # the path is the brute-force best of all 4^4 paths over the GPU's candidates
+    tau = O.transitions(inp["anchor"], g["cand_ids"], inp["U"], inp["V"])
+    bp, bs = O.brute_force_best(g["cand_lp"], tau)
+    assert np.array_equal(bp, g["path_idx"])
+    assert abs(float(bs[0]) - float(g["score"][0])) < 1e-4
+
+
+def test_fp32_small_rows():
+    rc = _recipe(base=1, batch=3, block=8, vocab=5000, layers=2)
+    sh = rc.shape
+    inp = synth.make_inputs(rc)
+    ref = O.draft_tail(inp, sh)
+    g = P.run_tail(P.shape_of(sh), P.upload_inputs(inp))
+    P.check_tail(sh, inp, ref, g)
+
+
+# ------------------------------------------------------------------ per-step calls
+
+
+@pytest.mark.parametrize("layers,raw", [(1, False), (5, False), (1, True)])
+def test_conv_step(layers, raw):
+    rc = _recipe(batch=5, block=8, hidden=5120, vocab=64, layers=layers)
+    sh = rc.shape
+    if raw:
+        sh.taps = "raw"
+        rc.conv_std = 0.002  # keeps raw taps near unit scale
+    inp = synth.make_inputs(rc, with_lm_head=True)
+    z_ref = O.conv_chain(inp["hidden"], inp["conv_w"], "bf16", 16, sh.taps)
+    z = P.run_conv(P.shape_of(sh), P.dev(inp["hidden"]), P.dev(inp["conv_w"]))
+    rep = P.check_conv(z, z_ref, max_ulps=1 if layers == 1 else None)
+    assert rep["conv_exact_frac"] > 0.95 and rep["conv_norm_rel"] < 2e-3
+    print(rep)
+
+
+def test_conv_step_block16_many_rows():
+    rc = _recipe(batch=40, block=16, hidden=1024, vocab=64, layers=5)
+    sh = rc.shape
+    inp = synth.make_inputs(rc)
+    z_ref = O.conv_chain(inp["hidden"], inp["conv_w"], "bf16", 16)
+    z = P.run_conv(P.shape_of(sh), P.dev(inp["hidden"]), P.dev(inp["conv_w"]))
+    P.check_conv(z, z_ref)
+
+
+def test_conv_shift_limit_exact():
+    # tap 0 dominant everywhere: z[t] = x[t - layers] exactly (the oracle's pinned special case)
+    B, T, H, L = 2, 8, 256, 3
+    rng = np.random.default_rng(0)
+    x = (rng.integers(1, 32, size=(B, T, H)) / 4.0).astype(np.float32)
+    xb = (x.view(np.uint32) >> 16).astype(np.uint16)
+    w = np.zeros((L, 2 * H // 16, H), np.float32)
+    w[:, 0::2, :] = 8.0
+    w[:, 1::2, :] = -8.0
+    wb = (w.view(np.uint32) >> 16).astype(np.uint16)
+    import block_drafter_dflash2_gb300 as df2
+    shape = df2.Shape.make(B, T, H, 64, 4, 32, L)
+    z = O.widen(P.run_conv(shape, P.dev(xb), P.dev(wb)))
+    exp = np.zeros_like(x)
+    exp[:, L:] = x[:, :T - L]
+    assert np.array_equal(z, exp)
+
+
+@pytest.mark.parametrize("M,V,H", [(8, 248_320 // 8, 5120), (256, 30_011, 512), (1, 777, 64)])
+def test_select_topk_step(M, V, H):
+    rc = _recipe(batch=M, block=1, hidden=H, vocab=V, layers=0)
+    sh = rc.shape
+    inp = synth.make_inputs(rc)
+    rows = inp["hidden"].reshape(M, H)
+    l32 = O.logits(rows, inp["lm_head"])
+    ids_o, vals_o, _ = O.topk_rows(l32, sh.top_k)
+    ref = dict(cand_ids=ids_o, cand_logit=vals_o, max_logit=l32.max(axis=1), lse=O.logsumexp_rows(l32))
+    ids, lp, lse = P.run_topk(P.shape_of(sh), P.dev(rows), P.dev(inp["lm_head"]))
+    rep = P.check_topk(ref, ids, lp, lse, rows, inp["lm_head"], sh.top_k)
+    print(M, V, H, "near-tie rows", len(rep["near_tie_rows"]))
+
+
+def test_select_topk_exact_ties_take_lower_ids():
+    # every logit is an integer; many exact ties: the kept ids must be the lowest ids among ties
+    M, H, V, K = 4, 64, 5000, 16
+    z = np.zeros((M, H), np.float32)
+    z[np.arange(M), np.arange(M)] = 1.0
+    W = np.zeros((V, H), np.float32)
+    W[:, :M] = (np.arange(V)[:, None] * np.array([3, 5, 7, 11])[None, :M]) % 13
+    zb = (z.view(np.uint32) >> 16).astype(np.uint16)
+    Wb = (W.view(np.uint32) >> 16).astype(np.uint16)
+    import block_drafter_dflash2_gb300 as df2
+    shape = df2.Shape.make(M, 1, H, V, K, 32, 0)
+    ids, lp, lse = P.run_topk(shape, P.dev(zb), P.dev(Wb))
+    l32 = O.logits(zb, Wb)
+    ids_o, _, _ = O.topk_rows(l32, K)
+    assert np.array_equal(ids, ids_o)
+    assert np.allclose(lse, O.logsumexp_rows(l32), atol=1e-4)
+
+
+@pytest.mark.parametrize("T,K,R", [(8, 16, 256), (1, 16, 256), (16, 4, 64), (32, 1, 16), (3, 16, 384)])
+def test_viterbi_step(T, K, R):
+    rng = np.random.default_rng(T * 1000 + K * 10 + R)
+    B, Vv = 6, 3000
+    sh = synth.Shape(batch=B, block=T, hidden=64, vocab=Vv, top_k=K, rank=R, layers=0)
+    U = synth.normal(5, 3, (Vv, R), 0.05)
+    V = synth.normal(5, 4, (Vv, R), 0.05)
+    cand = rng.integers(0, Vv, size=(B, T, K)).astype(np.int32)
+    cand[0, :, :] = cand[0, :1, :1]  # duplicated candidates everywhere in sequence 0
+    lp = (-np.sort(np.abs(rng.standard_normal((B, T, K))), axis=2) * 2).astype(np.float32)
+    anchor = rng.integers(0, Vv, size=B).astype(np.int32)
+    anchor[-1] = anchor[0]  # shared anchors
+    pid, pix, sc, err = P.run_viterbi(P.shape_of(sh), P.dev(anchor), P.dev(cand), P.dev(lp), P.dev(U), P.dev(V))
+    assert err == 0
+    P.check_walk(sh, anchor, U, V, cand, lp, pix, pid, sc)
+
+
+def test_greedy_walk_step():
+    rng = np.random.default_rng(3)
+    B, T, K, R, Vv = 5, 8, 16, 256, 2000
+    sh = synth.Shape(batch=B, block=T, hidden=64, vocab=Vv, top_k=K, rank=R, layers=0)
+    U = synth.normal(6, 3, (Vv, R), 0.3)
+    V = synth.normal(6, 4, (Vv, R), 0.3)
+    cand = rng.integers(0, Vv, size=(B, T, K)).astype(np.int32)
+    lp = (-np.sort(np.abs(rng.standard_normal((B, T, K))), axis=2)).astype(np.float32)
+    anchor = rng.integers(0, Vv, size=B).astype(np.int32)
+    shape = P.shape_of(sh, greedy=True)
+    pid, pix, sc, err = P.run_viterbi(shape, P.dev(anchor), P.dev(cand), P.dev(lp), P.dev(U), P.dev(V))
+    tau = O.transitions(anchor, cand, U, V)
+    gp, gs = O.greedy_walk(lp, tau)
+    vp, vs = O.viterbi(lp, tau)
+    assert np.array_equal(pix, gp)
+    assert np.allclose(sc, gs, atol=1e-4)
+    assert np.all(sc <= vs + 1e-4)
+
+
+def test_out_of_range_ids_set_the_error_word_and_clamp():
+    B, T, K, R, Vv = 2, 4, 4, 32, 100
+    sh = synth.Shape(batch=B, block=T, hidden=64, vocab=Vv, top_k=K, rank=R, layers=0)
+    U = synth.normal(7, 3, (Vv, R), 0.05)
+    V = synth.normal(7, 4, (Vv, R), 0.05)
+    cand = np.tile(np.arange(K, dtype=np.int32), (B, T, 1))
+    lp = np.zeros((B, T, K), np.float32)
+    anchor = np.array([5, Vv + 7], np.int32)
+    import block_drafter_dflash2_gb300 as df2
+    pid, pix, sc, err = P.run_viterbi(P.shape_of(sh), P.dev(anchor), P.dev(cand), P.dev(lp), P.dev(U), P.dev(V))
+    assert err == df2.DEVERR_ANCHOR_RANGE
+    cand[1, 2, 3] = -4
+    anchor[1] = 3
+    pid, pix, sc, err = P.run_viterbi(P.shape_of(sh), P.dev(anchor), P.dev(cand), P.dev(lp), P.dev(U), P.dev(V))
+    assert err == df2.DEVERR_CANDIDATE_RANGE
+    assert np.all((pid >= 0) & (pid < Vv))
+
+
+def test_argument_errors_return_before_launch():
+    import ctypes
+    import block_drafter_dflash2_gb300 as df2
+    rc = _recipe(batch=1, block=8, hidden=256, vocab=1000, layers=1)
+    shape = P.shape_of(rc.shape)
+    inp = synth.make_inputs(rc)
+    d = P.upload_inputs(inp)
+    ws = P.workspace(shape)
+    B, T, K = 1, 8, 16
+    o = [torch.empty((B, T), dtype=torch.int32, device="cuda"), torch.empty((B, T), dtype=torch.int32, device="cuda"),
+         torch.empty((B,), dtype=torch.float32, device="cuda")]
+    with pytest.raises(df2.DFlash2Error) as e:
+        df2.draft_tail(shape, d["hidden"], d["lm_head"], d["U"], d["V"], d["conv_w"], d["anchor"], *o,
+                       (ws.data_ptr(), ws.numel() - 1))
+    assert e.value.status == df2.ERR_WORKSPACE_TOO_SMALL
+    with pytest.raises(df2.DFlash2Error) as e:
+        df2.draft_tail(shape, d["hidden"].data_ptr() + 2, d["lm_head"], d["U"], d["V"], d["conv_w"], d["anchor"],
+                       *o, ws)
+    assert e.value.status == df2.ERR_INVALID_ARGUMENT
+    lib = df2.load()
+    st = lib.dflash2_draft_tail(ctypes.byref(shape), d["hidden"].data_ptr(), None, d["U"].data_ptr(),
+                                d["V"].data_ptr(), d["conv_w"].data_ptr(), d["anchor"].data_ptr(),
+                                o[0].data_ptr(), o[1].data_ptr(), o[2].data_ptr(), None, None, None,
+                                ws.data_ptr(), ws.numel(), None)
+    assert st == df2.ERR_INVALID_ARGUMENT
+    torch.cuda.synchronize()
+    assert df2.read_device_error(ws) == 0

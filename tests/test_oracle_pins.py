@@ -279,7 +279,7 @@ def test_viterbi_equals_brute_force(K, T):
                        for c in itertools.product(range(K), repeat=T)), reverse=True)
         assert abs(allv[1] - second[b]) < 1e-9
     gp, gs = O.greedy_walk(lp, tau)
-    assert np.all(gs <= bs + 1e-9)
+    assert np.all(gs <= bs + 1e-5)  # greedy score is fp32; the brute-force maximum is float64
 
 
 def test_viterbi_zero_transitions_is_per_slot_argmax():
