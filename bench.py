@@ -36,6 +36,18 @@ UNIT = "blocks/s"
 FLUSH_BYTES = 256 << 20
 
 
+def make_flush(torch, dev):
+    """L2 flush between steps: write a 256 MiB buffer (twice L2), then read another one, so the
+    step starts with a cold L2 that holds no dirty lines left by the flush itself."""
+    wbuf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    rbuf = torch.zeros(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flush():
+        wbuf.fill_(1)
+        rbuf.sum()
+    return flush
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -44,7 +56,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=2, help="workload (2: B=1 page shape)")
     ap.add_argument("--no-extra", action="store_true", help="skip the B=8/B=32 lines and the CPU baseline")
-    ap.add_argument("--kernel", choices=["lmhead"], default=None,
+    ap.add_argument("--kernel", choices=["lmhead", "conv"], default=None,
                     help="time one kernel alone (profiling case) instead of the whole tail")
     ap.add_argument("--rows", type=int, default=8, help="--kernel: rows of the contraction")
     ap.add_argument("--vocab", type=int, default=62080, help="--kernel: vocabulary size")
@@ -195,7 +207,7 @@ def run_ours(args, rank, world, local_rank):
     d = {k: up(inp[k]) for k in ("hidden", "lm_head", "U", "V", "conv_w", "anchor")}
     shape = df2.Shape.make(B, T, H, sh.vocab, K, sh.rank, sh.layers)
     ws = torch.zeros(df2.workspace_size(shape), dtype=torch.uint8, device=dev)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = make_flush(torch, dev)
     out = dict(pid=torch.empty((B, T), dtype=torch.int32, device=dev),
                pix=torch.empty((B, T), dtype=torch.int32, device=dev),
                score=torch.empty((B,), dtype=torch.float32, device=dev))
@@ -210,11 +222,11 @@ def run_ours(args, rank, world, local_rank):
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
         with torch.cuda.stream(stream):
             for _ in range(warm):
-                flush.fill_(1)
+                flush()
                 fn()
             torch.cuda.synchronize(dev)
             for e0, e1 in evs:
-                flush.fill_(1)
+                flush()
                 e0.record(stream)
                 fn()
                 e1.record(stream)
@@ -234,7 +246,7 @@ def run_ours(args, rank, world, local_rank):
     clocks.start()
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
-            flush.fill_(1)
+            flush()
             graph.replay()
     torch.cuda.synchronize(dev)
     if world > 1:
@@ -254,16 +266,28 @@ def run_ours(args, rank, world, local_rank):
         t_max = float(t.item())
     clk = clocks.stop()
 
-    # dominant kernel on its own: the LM-head contraction with its fused epilogue
+    def graphed(fn):
+        """fn captured in its own CUDA graph: times the kernels, not the host call."""
+        with torch.cuda.stream(stream):
+            fn()
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        return g.replay
+
+    # each stage on its own; the dominant kernel (the LM-head contraction with its fused
+    # epilogue) gives the roofline figure
     z = torch.empty_like(d["hidden"])
-    df2.conv(shape, d["hidden"], d["conv_w"], z, ws, stream=stream)
-    lm_ms = timed(lambda: df2.lmhead_partials(shape, z, d["lm_head"], ws, stream=stream), args.steps, 3)
-    conv_ms = timed(lambda: df2.conv(shape, d["hidden"], d["conv_w"], z, ws, stream=stream), min(args.steps, 50), 3)
     ids = torch.empty((M, K), dtype=torch.int32, device=dev)
     lp = torch.empty((M, K), dtype=torch.float32, device=dev)
-    merge_ms = timed(lambda: df2.merge_partials(shape, ids, lp, None, ws, stream=stream), min(args.steps, 50), 3)
-    walk_ms = timed(lambda: df2.viterbi(shape, d["anchor"], ids, lp, d["U"], d["V"], out["pid"], out["pix"],
-                                        out["score"], ws, stream=stream), min(args.steps, 50), 3)
+    conv_ms = timed(graphed(lambda: df2.conv(shape, d["hidden"], d["conv_w"], z, ws, stream=stream)),
+                    min(args.steps, 50), 3)
+    lm_ms = timed(graphed(lambda: df2.lmhead_partials(shape, z, d["lm_head"], ws, stream=stream)), args.steps, 3)
+    merge_ms = timed(graphed(lambda: df2.merge_partials(shape, ids, lp, None, ws, stream=stream)),
+                     min(args.steps, 50), 3)
+    walk_ms = timed(graphed(lambda: df2.viterbi(shape, d["anchor"], ids, lp, d["U"], d["V"], out["pid"], out["pix"],
+                                                out["score"], ws, stream=stream)), min(args.steps, 50), 3)
 
     # end to end through the public call, host buffers in and out
     h_hidden = torch.from_numpy(inp["hidden"].view(np.int16)).pin_memory()
@@ -314,14 +338,16 @@ def run_ours(args, rank, world, local_rank):
                 call2()
             ms2 = timed(g2.replay, args.steps, 3)
             z2 = torch.empty_like(hb_d)
-            df2.conv(shp2, hb_d, d["conv_w"], z2, ws2, stream=stream)
-            lm2 = timed(lambda: df2.lmhead_partials(shp2, z2, d["lm_head"], ws2, stream=stream), args.steps, 3)
+            cv2 = timed(graphed(lambda: df2.conv(shp2, hb_d, d["conv_w"], z2, ws2, stream=stream)), 20, 3)
+            lm2 = timed(graphed(lambda: df2.lmhead_partials(shp2, z2, d["lm_head"], ws2, stream=stream)),
+                        args.steps, 3)
             us = statistics.mean(ms2) * 1e3
             lmu = statistics.mean(lm2) * 1e3
             roof = tail_roofline_us(sh, b2 * T, bw, tf)
             extra[f"B={b2}"] = {
                 "us_per_call": round(us, 2), "blocks_per_s": round(b2 / (us * 1e-6), 1),
                 "tail_roofline_frac": round(roof / us, 4), "lmhead_us": round(lmu, 2),
+                "conv_us": round(statistics.mean(cv2) * 1e3, 2),
                 "lmhead_hbm_gbs": round(lmhead_alg_bytes(sh, b2 * T) / (lmu * 1e-6) / 1e9, 1),
                 "lmhead_tflops": round(2.0 * b2 * T * H * sh.vocab / (lmu * 1e-6) / 1e12, 1)}
 
@@ -338,7 +364,7 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": rc.name, "batch": B, "block": T, "hidden": H, "vocab": sh.vocab, "top_k": K,
                    "rank": sh.rank, "conv_layers": sh.layers, "parallelism": "replicas" if world > 1 else "single",
                    "timing": "CUDA graph replay, CUDA events per step",
-                   "l2": "flushed before every step (256 MiB write)"},
+                   "l2": "flushed before every step (256 MiB write, then a 256 MiB read)"},
         "us_per_call": round(us, 2),
         "us_per_call_p10_p90": [round(float(np.percentile(step_ms, 10)) * 1e3, 2),
                                 round(float(np.percentile(step_ms, 90)) * 1e3, 2)],
@@ -369,26 +395,38 @@ def run_kernel_case(args):
     import block_drafter_dflash2_gb300 as df2
     df2.load()
     dev = torch.device("cuda", 0)
-    rc = synth.scaled_recipe(synth.recipe(2), batch=args.rows, block=1, vocab=args.vocab, layers=0)
+    conv = args.kernel == "conv"
+    rows, block = (args.rows // 8, 8) if conv else (args.rows, 1)
+    rc = synth.scaled_recipe(synth.recipe(2), batch=rows, block=block, vocab=args.vocab if not conv else 64,
+                             layers=5 if conv else 0)
     sh = rc.shape
     inp = synth.make_inputs(rc)
     z = torch.from_numpy(inp["hidden"].view(np.int16)).to(dev)
     w = torch.from_numpy(inp["lm_head"].view(np.int16)).to(dev)
-    shape = df2.Shape.make(args.rows, 1, sh.hidden, sh.vocab, sh.top_k, sh.rank, 0)
+    cw = torch.from_numpy(inp["conv_w"].view(np.int16)).to(dev)
+    y = torch.empty_like(z)
+    shape = df2.Shape.make(rows, block, sh.hidden, sh.vocab, sh.top_k, sh.rank, sh.layers)
     ws = torch.zeros(df2.workspace_size(shape), dtype=torch.uint8, device=dev)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = make_flush(torch, dev)
     ms = []
     for i in range(args.warmup + args.steps):
-        flush.fill_(1)
+        flush()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        df2.lmhead_partials(shape, z, w, ws)
+        if conv:
+            df2.conv(shape, z, cw, y, ws)
+        else:
+            df2.lmhead_partials(shape, z, w, ws)
         e1.record()
         torch.cuda.synchronize()
         if i >= args.warmup:
             ms.append(e0.elapsed_time(e1))
     assert df2.read_device_error(ws) == 0
     us = statistics.mean(ms) * 1e3
+    if conv:
+        print(json.dumps({"kernel": "conv (5 layers)", "rows": rows * block, "hidden": sh.hidden, "us": round(us, 2)}),
+              flush=True)
+        return
     print(json.dumps({"kernel": "lmhead_partials", "rows": args.rows, "vocab": sh.vocab, "hidden": sh.hidden,
                       "us": round(us, 2), "alg_gbs": round(lmhead_alg_bytes(sh, args.rows) / (us * 1e-6) / 1e9, 1),
                       "tflops": round(2.0 * args.rows * sh.hidden * sh.vocab / (us * 1e-6) / 1e12, 1)}), flush=True)

@@ -64,8 +64,10 @@ struct Plan {
   bool bf16;
   size_t esz;
   int n_rc;
+  int a_tail_rows;  // rows of the last 128-row chunk, rounded up to 8
   int lm_parts;
   int conv_parts;
+  int chain_grid;  // > 0: all conv layers in one cooperative launch of this many CTAs
   bool raw, greedy;
 };
 
@@ -101,13 +103,19 @@ dflash2_status_t make_plan(const dflash2_shape_t* s, Plan& p) {
   const int p_units = (p.P + 15) / 16;
   if (p.bf16) {
     p.n_rc = (p.M + 127) / 128;
+    p.a_tail_rows = (p.M % 128 == 0) ? 128 : ((p.M % 128 + 7) / 8) * 8;
     const int per = sms / p.n_rc > 0 ? sms / p.n_rc : 1;
     p.lm_parts = per < v_units ? per : v_units;
     p.conv_parts = per < p_units ? per : p_units;
+    const int groups = p.H / 16;
+    const int grid = sms < groups ? sms : groups;
+    p.chain_grid = (p.M <= 64 && (groups + grid - 1) / grid <= 4) ? grid : 0;
   } else {
     p.n_rc = 1;
+    p.a_tail_rows = 0;
     p.lm_parts = sms < v_units ? sms : v_units;
     p.conv_parts = 0;
+    p.chain_grid = 0;
   }
   if (p.lm_parts > 1024) p.lm_parts = 1024;
   return DFLASH2_OK;
@@ -117,6 +125,7 @@ size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Ws {
   int32_t* err;
+  unsigned* bar;
   void* conv0;
   void* conv1;
   float* part_val;
@@ -138,6 +147,7 @@ Ws carve(const Plan& p, void* base) {
   };
   const size_t act = (size_t)p.M * p.H * p.esz;
   w.err = static_cast<int32_t*>(take(256));
+  w.bar = static_cast<unsigned*>(take(256));
   w.conv0 = take(act);
   w.conv1 = take(act);
   w.part_val = static_cast<float*>(take((size_t)p.lm_parts * p.M * 16 * 4));
@@ -165,17 +175,20 @@ dflash2_status_t run_conv(const Plan& p, const void* x, const void* conv_w, void
                           cudaStream_t s) {
   const size_t act = (size_t)p.M * p.H * p.esz;
   if (p.NL == 0) return cuda_status(cudaMemcpyAsync(y, x, act, cudaMemcpyDeviceToDevice, s));
+  if (p.bf16 && p.chain_grid > 0)
+    return cuda_status(df::launch_conv_chain_small(x, conv_w, w.conv0, w.conv1, y, p.M, p.H, p.T, p.NL,
+                                                   p.raw ? 1 : 0, w.bar, w.err, p.chain_grid, s));
   const void* cur = x;
   for (int l = 0; l < p.NL; ++l) {
     void* out = (l == p.NL - 1) ? y : ((l % 2 == 0) ? w.conv0 : w.conv1);
     const char* wl = static_cast<const char*>(conv_w) + (size_t)l * p.P * p.H * p.esz;
     if (p.bf16) {
-      CUtensorMap ma, mb128, mb16;
-      if (!encode_bf16_2d(&ma, cur, p.H, p.M, 128) || !encode_bf16_2d(&mb128, wl, p.H, p.P, 128) ||
-          !encode_bf16_2d(&mb16, wl, p.H, p.P, 16))
+      CUtensorMap ma, mat, mb128, mb16;
+      if (!encode_bf16_2d(&ma, cur, p.H, p.M, 128) || !encode_bf16_2d(&mat, cur, p.H, p.M, p.a_tail_rows) ||
+          !encode_bf16_2d(&mb128, wl, p.H, p.P, 128) || !encode_bf16_2d(&mb16, wl, p.H, p.P, 16))
         return DFLASH2_ERR_CUDA;
-      TcGemmArgs a{p.M, p.H, p.P, p.n_rc, p.conv_parts, w.err};
-      if (df::launch_conv_layer_bf16(ma, mb128, mb16, a, cur, out, p.T, p.raw ? 1 : 0, s) != cudaSuccess)
+      TcGemmArgs a{p.M, p.H, p.P, p.n_rc, p.conv_parts, p.a_tail_rows, w.err};
+      if (df::launch_conv_layer_bf16(ma, mat, mb128, mb16, a, cur, out, p.T, p.raw ? 1 : 0, s) != cudaSuccess)
         return DFLASH2_ERR_CUDA;
     } else {
       if (df::launch_conv_layer_f32(static_cast<const float*>(cur), reinterpret_cast<const float*>(wl),
@@ -188,13 +201,13 @@ dflash2_status_t run_conv(const Plan& p, const void* x, const void* conv_w, void
 }
 
 dflash2_status_t run_partials(const Plan& p, const void* rows, const void* lm_head, const Ws& w, cudaStream_t s) {
-  TcGemmArgs a{p.M, p.H, p.V, p.n_rc, p.lm_parts, w.err};
+  TcGemmArgs a{p.M, p.H, p.V, p.n_rc, p.lm_parts, p.a_tail_rows, w.err};
   if (p.bf16) {
-    CUtensorMap ma, mb128, mb16;
-    if (!encode_bf16_2d(&ma, rows, p.H, p.M, 128) || !encode_bf16_2d(&mb128, lm_head, p.H, p.V, 128) ||
-        !encode_bf16_2d(&mb16, lm_head, p.H, p.V, 16))
+    CUtensorMap ma, mat, mb128, mb16;
+    if (!encode_bf16_2d(&ma, rows, p.H, p.M, 128) || !encode_bf16_2d(&mat, rows, p.H, p.M, p.a_tail_rows) ||
+        !encode_bf16_2d(&mb128, lm_head, p.H, p.V, 128) || !encode_bf16_2d(&mb16, lm_head, p.H, p.V, 16))
       return DFLASH2_ERR_CUDA;
-    if (df::launch_lmhead_topk_bf16(ma, mb128, mb16, a, w.part_val, w.part_id, w.part_ms, s) != cudaSuccess)
+    if (df::launch_lmhead_topk_bf16(ma, mat, mb128, mb16, a, w.part_val, w.part_id, w.part_ms, s) != cudaSuccess)
       return DFLASH2_ERR_CUDA;
   } else {
     if (df::launch_lmhead_topk_f32(static_cast<const float*>(rows), static_cast<const float*>(lm_head), a,

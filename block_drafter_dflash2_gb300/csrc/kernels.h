@@ -10,14 +10,23 @@
 namespace df {
 
 // tcgen05 GEMM + top-K/lse partials (bf16). grid = n_rc * parts.
-cudaError_t launch_lmhead_topk_bf16(const CUtensorMap& a, const CUtensorMap& b128, const CUtensorMap& b16,
+cudaError_t launch_lmhead_topk_bf16(const CUtensorMap& a, const CUtensorMap& a_tail, const CUtensorMap& b128,
+                                    const CUtensorMap& b16,
                                     const TcGemmArgs& args, float* part_val, int32_t* part_id,
                                     float* part_ms, cudaStream_t s);
 
 // tcgen05 GEMM + conv-layer epilogue (bf16): y = mix(x) with taps = x * W^T.
-cudaError_t launch_conv_layer_bf16(const CUtensorMap& a, const CUtensorMap& b128, const CUtensorMap& b16,
+cudaError_t launch_conv_layer_bf16(const CUtensorMap& a, const CUtensorMap& a_tail, const CUtensorMap& b128,
+                                   const CUtensorMap& b16,
                                    const TcGemmArgs& args, const void* x, void* y, int T, int raw,
                                    cudaStream_t s);
+
+// All conv layers in one cooperative launch for M <= 64 rows (bf16); `grid` CTAs, each owning
+// a contiguous range of at most 4 channel groups. Zeroes *bar_count on the stream first.
+size_t conv_chain_small_smem(int H);
+cudaError_t launch_conv_chain_small(const void* x, const void* conv_w, void* buf0, void* buf1, void* z, int M,
+                                    int H, int T, int NL, int raw, unsigned* bar_count, int32_t* err, int grid,
+                                    cudaStream_t s);
 
 // fp32 instantiations (small sizes).
 cudaError_t launch_conv_layer_f32(const float* x, const float* w, float* y, int M, int H, int T, int raw,

@@ -7,8 +7,9 @@ namespace df {
 
 namespace {
 template <class Epi>
-cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b128, const CUtensorMap& b16,
-                        const TcGemmArgs& args, const typename Epi::Params& ep, cudaStream_t s) {
+cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& a_tail, const CUtensorMap& b128,
+                        const CUtensorMap& b16, const TcGemmArgs& args, const typename Epi::Params& ep,
+                        cudaStream_t s) {
   static int configured_for = -1;  // device ordinal the smem attribute was set for
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -19,24 +20,24 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b128, const CUt
     configured_for = dev;
   }
   const int grid = args.n_rc * args.parts;
-  tc_gemm_kernel<Epi><<<grid, kGemmThreads, kGemmSmemBytes, s>>>(a, b128, b16, args, ep);
+  tc_gemm_kernel<Epi><<<grid, kGemmThreads, kGemmSmemBytes, s>>>(a, a_tail, b128, b16, args, ep);
   return cudaGetLastError();
 }
 }  // namespace
 
-cudaError_t launch_lmhead_topk_bf16(const CUtensorMap& a, const CUtensorMap& b128, const CUtensorMap& b16,
-                                    const TcGemmArgs& args, float* part_val, int32_t* part_id,
-                                    float* part_ms, cudaStream_t s) {
+cudaError_t launch_lmhead_topk_bf16(const CUtensorMap& a, const CUtensorMap& a_tail, const CUtensorMap& b128,
+                                    const CUtensorMap& b16, const TcGemmArgs& args, float* part_val,
+                                    int32_t* part_id, float* part_ms, cudaStream_t s) {
   EpiTopK::Params ep{part_val, part_id, part_ms, args.M};
-  return launch_gemm<EpiTopK>(a, b128, b16, args, ep, s);
+  return launch_gemm<EpiTopK>(a, a_tail, b128, b16, args, ep, s);
 }
 
-cudaError_t launch_conv_layer_bf16(const CUtensorMap& a, const CUtensorMap& b128, const CUtensorMap& b16,
-                                   const TcGemmArgs& args, const void* x, void* y, int T, int raw,
-                                   cudaStream_t s) {
+cudaError_t launch_conv_layer_bf16(const CUtensorMap& a, const CUtensorMap& a_tail, const CUtensorMap& b128,
+                                   const CUtensorMap& b16, const TcGemmArgs& args, const void* x, void* y, int T,
+                                   int raw, cudaStream_t s) {
   EpiConv::Params ep{reinterpret_cast<const __nv_bfloat16*>(x), reinterpret_cast<__nv_bfloat16*>(y), args.M,
                      args.K, T, raw};
-  return launch_gemm<EpiConv>(a, b128, b16, args, ep, s);
+  return launch_gemm<EpiConv>(a, a_tail, b128, b16, args, ep, s);
 }
 
 }  // namespace df

@@ -1,7 +1,12 @@
-// Cross-partition merge: each column partition of the LM-head GEMM left, per row, its
-// top-16 (logit desc, id asc) and its (max, sum of exp(l - max)). One warp per row merges
-// them: lse = M + log(sum_p s_p * exp(m_p - M)), then K rounds of a warp-wide arg-max over
-// the heads of the sorted partition lists (ties to the lower id).
+// Cross-partition merge: each column partition of the LM-head contraction left, per row, its
+// top-16 (logit desc, id asc) and its (max, sum of exp(l - max)). One CTA per row stages the
+// row's partials in shared memory with one batch of 16-byte loads, reduces
+// lse = M + log(sum_p s_p * exp(m_p - M)) across the block, and warp 0 then takes K rounds of
+// a warp-wide arg-max over the heads of the sorted partition lists (ties to the lower id).
+// Each lane owns the lists p = lane (mod 32) and caches its best head; a round is one
+// redux.sync max over an order-preserving key of the logit, a ballot of the lanes holding it
+// and a redux.sync min over their ids; then only the winning lane rescans its own lists.
+// The partials are staged with cp.async so every load of a row is in flight at once.
 #include <math.h>
 
 #include "kernels.h"
@@ -9,48 +14,86 @@
 namespace df {
 
 namespace {
-constexpr int kRowsPerBlock = 4;
+constexpr int kThreads = 128;
 constexpr int kMaxParts = 1024;
 
 __device__ __forceinline__ bool better(float v, int32_t id, float bv, int32_t bid) {
   return v > bv || (v == bv && id < bid);
 }
 
-__global__ void __launch_bounds__(32 * kRowsPerBlock)
-    topk_merge_kernel(const float* __restrict__ part_val, const int32_t* __restrict__ part_id,
+// Unsigned key with the same order as the float (negative values reversed); 0 = no entry.
+__device__ __forceinline__ uint32_t order_key(float v) {
+  const uint32_t u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
+               "l"(gmem_src)
+               : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads)
+    topk_merge_kernel(const float4* __restrict__ part_val, const int4* __restrict__ part_id,
                       const float2* __restrict__ part_ms, int parts, int M, int K, int32_t* __restrict__ cand_ids,
                       float* __restrict__ cand_lp, float* __restrict__ lse_out) {
-  __shared__ uint8_t head[kRowsPerBlock][kMaxParts];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * kRowsPerBlock + warp;
-  if (row >= M) return;  // warp-uniform
-  for (int p = lane; p < parts; p += 32) head[warp][p] = 0;
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  float* sv = reinterpret_cast<float*>(smem_raw);              // [parts][16]
+  int32_t* si = reinterpret_cast<int32_t*>(sv + parts * 16);   // [parts][16]
+  uint8_t* head = reinterpret_cast<uint8_t*>(si + parts * 16);  // [parts]
+  __shared__ float red_m[kThreads / 32], red_s[kThreads / 32];
+  __shared__ float lse_s;
+  const int row = blockIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  for (int e = tid; e < parts * 4; e += kThreads) {
+    const int p = e >> 2, q = e & 3;
+    const size_t src = ((size_t)p * M + row) * 4 + q;
+    cp_async16(reinterpret_cast<float4*>(sv) + e, part_val + src);
+    cp_async16(reinterpret_cast<int4*>(si) + e, part_id + src);
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  for (int p = tid; p < parts; p += kThreads) head[p] = 0;
 
   float m = -INFINITY;
-  for (int p = lane; p < parts; p += 32) m = fmaxf(m, part_ms[(size_t)p * M + row].x);
+  for (int p = tid; p < parts; p += kThreads) m = fmaxf(m, part_ms[(size_t)p * M + row].x);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) red_m[warp] = m;
+  __syncthreads();
+  m = red_m[0];
+#pragma unroll
+  for (int w = 1; w < kThreads / 32; ++w) m = fmaxf(m, red_m[w]);
   float s = 0.f;
-  for (int p = lane; p < parts; p += 32) {
+  for (int p = tid; p < parts; p += kThreads) {
     const float2 ms = part_ms[(size_t)p * M + row];
     if (ms.y > 0.f) s += ms.y * expf(ms.x - m);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  const float lse = m + logf(s);
-  if (lane == 0 && lse_out) lse_out[row] = lse;
-  __syncwarp();
+  if (lane == 0) red_s[warp] = s;
+  __syncthreads();
+  if (tid == 0) {
+    float t = 0.f;
+    for (int w = 0; w < kThreads / 32; ++w) t += red_s[w];
+    lse_s = m + logf(t);
+    if (lse_out) lse_out[row] = lse_s;
+  }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  __syncthreads();
+  if (warp != 0) return;
+  const float lse = lse_s;
 
-  for (int k = 0; k < K; ++k) {
-    float bv = -INFINITY;
-    int32_t bid = 0x7fffffff;
-    int bp = -1;
+  auto rescan = [&](float& bv, int32_t& bid, int& bp) {
+    bv = -INFINITY;
+    bid = 0x7fffffff;
+    bp = -1;
     for (int p = lane; p < parts; p += 32) {
-      const int h = head[warp][p];
+      const int h = head[p];
       if (h < 16) {
-        const size_t at = ((size_t)p * M + row) * 16 + h;
-        const float v = part_val[at];
-        const int32_t id = part_id[at];
+        const float v = sv[p * 16 + h];
+        const int32_t id = si[p * 16 + h];
         if (bp < 0 || better(v, id, bv, bid)) {
           bv = v;
           bid = id;
@@ -58,21 +101,23 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock)
         }
       }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int32_t oid = __shfl_xor_sync(0xffffffffu, bid, o);
-      const int op = __shfl_xor_sync(0xffffffffu, bp, o);
-      if (op >= 0 && (bp < 0 || better(ov, oid, bv, bid))) {
-        bv = ov;
-        bid = oid;
-        bp = op;
-      }
-    }
-    if (bp >= 0 && lane == (bp & 31)) head[warp][bp] += 1;
-    if (lane == 0) {
+  };
+  float bv;
+  int32_t bid;
+  int bp;
+  rescan(bv, bid, bp);
+  for (int k = 0; k < K; ++k) {
+    const uint32_t key = bp >= 0 ? order_key(bv) : 0u;
+    const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
+    const bool tied = key == kmax && bp >= 0;
+    const uint32_t wid = __reduce_min_sync(0xffffffffu, tied ? (uint32_t)bid : 0xffffffffu);
+    const uint32_t win = __ballot_sync(0xffffffffu, tied && (uint32_t)bid == wid);  // ids are unique
+    const int wl = __ffs(win) - 1;
+    if (lane == wl) {
       cand_ids[(size_t)row * K + k] = bid;
       cand_lp[(size_t)row * K + k] = bv - lse;
+      head[bp] += 1;
+      rescan(bv, bid, bp);
     }
     __syncwarp();
   }
@@ -82,9 +127,15 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock)
 cudaError_t launch_topk_merge(const float* part_val, const int32_t* part_id, const float* part_ms, int parts,
                               int M, int K, int32_t* cand_ids, float* cand_lp, float* lse, cudaStream_t s) {
   if (parts > kMaxParts) return cudaErrorInvalidValue;
-  const int grid = (M + kRowsPerBlock - 1) / kRowsPerBlock;
-  topk_merge_kernel<<<grid, 32 * kRowsPerBlock, 0, s>>>(part_val, part_id, reinterpret_cast<const float2*>(part_ms),
-                                                        parts, M, K, cand_ids, cand_lp, lse);
+  const size_t smem = (size_t)parts * 16 * 8 + parts;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  topk_merge_kernel<<<M, kThreads, smem, s>>>(reinterpret_cast<const float4*>(part_val),
+                                               reinterpret_cast<const int4*>(part_id),
+                                               reinterpret_cast<const float2*>(part_ms), parts, M, K, cand_ids,
+                                               cand_lp, lse);
   return cudaGetLastError();
 }
 

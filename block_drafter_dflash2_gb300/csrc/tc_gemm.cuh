@@ -12,9 +12,12 @@
 //
 // Roles (192 threads): warp 0 = TMA producer (one thread), warp 1 = MMA issuer (one thread)
 // and TMEM owner, warps 2..5 = epilogue (thread = TMEM lane = row). Shared memory holds a
-// kStages-deep ring of (A 128x64, B 128x64) bf16 tiles in the 128-byte swizzled K-major
-// layout; TMEM holds two 128-column fp32 accumulators so the epilogue of tile t overlaps
-// the MMAs of tile t+1.
+// ring of (A, B) bf16 stages, K = 64 each, in the 128-byte swizzled K-major layout. The A
+// box of the last row chunk covers only its real rows (rounded up to 8), so a small M does
+// not pay for TMA zero-fill, and the ring is cut into as many stages as fit, so small tiles
+// keep many more loads in flight. The MMA reads 128 A rows regardless; rows past the box hold
+// stale data and only feed TMEM lanes no epilogue thread reads. TMEM holds two 128-column
+// fp32 accumulators so the epilogue of tile t overlaps the MMAs of tile t+1.
 #pragma once
 
 #include "ptx.cuh"
@@ -25,13 +28,13 @@ namespace df {
 constexpr int kBK = 64;   // K per stage: one 128-byte swizzle row of bf16
 constexpr int kBM = 128;  // rows per tile (MMA M)
 constexpr int kBN = 128;  // widest tile (MMA N)
-constexpr int kStages = 6;
-constexpr int kTileABytes = kBM * kBK * 2;
-constexpr int kTileBBytes = kBN * kBK * 2;
-constexpr int kStageBytes = kTileABytes + kTileBBytes;
+constexpr int kMaxStages = 48;
+constexpr int kRingBytes = 200 * 1024;           // smem ring, split into as many stages as fit
+constexpr int kASlackBytes = kBM * kBK * 2;       // the MMA always reads 128 A rows from a stage
+constexpr int kBarrierBytes = 1024;
 constexpr int kGemmThreads = 192;
 constexpr int kTmemCols = 2 * kBN;
-constexpr int kGemmSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int kGemmSmemBytes = 1024 /*align*/ + kBarrierBytes + kRingBytes + kASlackBytes;
 
 struct TileRange {
   int u0, u1;      // unit range [u0, u1) of 16 columns
@@ -49,20 +52,38 @@ DF_DEV TileRange tile_range(const TcGemmArgs& a, int part) {
   return r;
 }
 
+// Stage geometry of one CTA: the A box is the row chunk's real rows (padded to 8; 128 for full
+// chunks), the B tile is as wide as this CTA's widest tile. Stages are as many as fit the ring.
+struct StageGeom {
+  uint32_t a_bytes, stride;
+  int stages;
+};
+
+DF_DEV StageGeom stage_geom(const TcGemmArgs& a, int rc, const TileRange& tr) {
+  StageGeom g;
+  const int rows = (rc == a.n_rc - 1) ? a.a_tail_rows : kBM;
+  g.a_bytes = (uint32_t)rows * kBK * 2;
+  const int nmax = min(8, tr.u1 - tr.u0) * 16;
+  g.stride = (g.a_bytes + (uint32_t)nmax * kBK * 2 + 1023u) & ~1023u;
+  g.stages = min(kMaxStages, (int)(kRingBytes / g.stride));
+  return g;
+}
+
 template <class Epi>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b128,
-                   const __grid_constant__ CUtensorMap map_b16, const TcGemmArgs args,
-                   const typename Epi::Params ep) {
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_a_tail,
+                   const __grid_constant__ CUtensorMap map_b128, const __grid_constant__ CUtensorMap map_b16,
+                   const TcGemmArgs args, const typename Epi::Params ep) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
-  uint64_t* empty = full + kStages;
-  uint64_t* tfull = empty + kStages;
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(base);
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* tfull = empty + kMaxStages;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint8_t* ring = base + kBarrierBytes;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -70,10 +91,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int part = blockIdx.x / args.n_rc;
   if (part >= args.parts) return;  // whole CTA idle (uniform)
   const TileRange tr = tile_range(args, part);
+  const StageGeom sg = stage_geom(args, rc, tr);
   const int kblocks = args.K / kBK;
+  const bool tail_chunk = (rc == args.n_rc - 1);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < sg.stages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -89,8 +112,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
-  if (threadIdx.x == 32 * 0) {
-    tma_prefetch_desc(&map_a);
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(tail_chunk ? &map_a_tail : &map_a);
     tma_prefetch_desc(&map_b128);
     tma_prefetch_desc(&map_b16);
   }
@@ -104,33 +127,34 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // ---------------- TMA producer
       const uint64_t pol_a = l2_policy_evict_last();   // row tiles are re-read for every column tile
       const uint64_t pol_b = l2_policy_evict_first();  // column tiles (weights) stream through once
+      const CUtensorMap* ma = tail_chunk ? &map_a_tail : &map_a;
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t issued = 0, issued_phase = 0;  // per-stage bits: ever issued / parity of last issue
+      uint64_t issued = 0, issued_phase = 0;  // per-stage bits: ever issued / parity of last issue
       bool ok = true;
       for (int t = 0; t < tr.num_tiles && ok; ++t) {
         const int cu0 = tr.u0 + t * 8;
         const int nu = min(8, tr.u1 - cu0);
         const int n0 = cu0 * 16;
-        const uint32_t bytes = kTileABytes + nu * 16 * kBK * 2;
+        const uint32_t bytes = sg.a_bytes + (uint32_t)nu * 16 * kBK * 2;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, args.err, abort_flag)) {
             ok = false;
             break;
           }
-          uint8_t* sa = smem + stage * kStageBytes;
-          uint8_t* sb = sa + kTileABytes;
+          uint8_t* sa = ring + (size_t)stage * sg.stride;
+          uint8_t* sb = sa + sg.a_bytes;
           mbar_arrive_expect_tx(&full[stage], bytes);
-          tma_load_2d(sa, &map_a, &full[stage], kb * kBK, rc * kBM, pol_a);
+          tma_load_2d(sa, ma, &full[stage], kb * kBK, rc * kBM, pol_a);
           if (nu == 8) {
             tma_load_2d(sb, &map_b128, &full[stage], kb * kBK, n0, pol_b);
           } else {
             for (int j = 0; j < nu; ++j)
               tma_load_2d(sb + j * 16 * kBK * 2, &map_b16, &full[stage], kb * kBK, n0 + 16 * j, pol_b);
           }
-          issued |= 1u << stage;
-          issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
-          if (++stage == kStages) {
+          issued |= 1ull << stage;
+          issued_phase = (issued_phase & ~(1ull << stage)) | ((uint64_t)phase << stage);
+          if (++stage == sg.stages) {
             stage = 0;
             phase ^= 1u;
           }
@@ -138,8 +162,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       if (!ok) {
         // Aborted: let every copy still in flight land before the CTA can exit.
-        for (int s = 0; s < kStages; ++s)
-          if (issued & (1u << s)) mbar_wait(&full[s], (issued_phase >> s) & 1u, args.err, nullptr);
+        for (int s = 0; s < sg.stages; ++s)
+          if (issued & (1ull << s)) mbar_wait(&full[s], (uint32_t)(issued_phase >> s) & 1u, args.err, nullptr);
       }
     }
   } else if (warp == 1) {
@@ -162,14 +186,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_u32(smem + stage * kStageBytes);
+          const uint32_t sa = smem_u32(ring + (size_t)stage * sg.stride);
           const uint64_t da = sdesc_k_sw128(sa);
-          const uint64_t db = sdesc_k_sw128(sa + kTileABytes);
+          const uint64_t db = sdesc_k_sw128(sa + sg.a_bytes);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)  // 16 bf16 = 32 B per MMA along K: +2 in 16-B units
             umma_bf16(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
           umma_commit(&empty[stage]);
-          if (++stage == kStages) {
+          if (++stage == sg.stages) {
             stage = 0;
             phase ^= 1u;
           }

@@ -11,6 +11,7 @@ struct TcGemmArgs {
   int n_total;   // columns in total
   int n_rc;      // row chunks of 128
   int parts;     // column partitions per row chunk
+  int a_tail_rows;  // TMA box rows of the last row chunk: its rows rounded up to 8 (128 if full)
   int32_t* err;  // device error word
 };
 

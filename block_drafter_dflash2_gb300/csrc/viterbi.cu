@@ -2,8 +2,8 @@
 //
 // For slot boundary t the previous candidates are the anchor (t = 0, repeated K times) or
 // slot t-1's candidates; the current ones are slot t's. Warp t % 8 gathers the 16 U-rows
-// (previous) and 16 V-rows (current) with 128-bit loads into padded shared memory, R/16
-// k-steps at a time in chunks of up to 128 columns, and forms the 16x16 tile
+// (previous) and 16 V-rows (current) with 16-byte cp.async copies (all in flight at once)
+// into padded shared memory, in chunks of up to 256 columns, and forms the 16x16 tile
 // tau_t(i, j) = <U[prev_i], V[cur_j]> with mma.sync m16n8k16 (bf16 in, fp32 accumulate).
 // Warp 0 then runs the recursion over the tiles: lane j holds delta(j); each step takes,
 // for every j, the max over i of delta(i) + tau(i, j) with the lowest i on ties, adds
@@ -19,8 +19,8 @@ namespace df {
 namespace {
 constexpr int kWarps = 8;
 constexpr int kKP = 16;         // candidate slots per tile (K padded to 16)
-constexpr int kRChunk = 128;    // embedding columns staged per pass
-constexpr int kRowPad = kRChunk + 8;  // bf16 per staged row: 272 B, keeps ldmatrix conflict-free
+constexpr int kRChunk = 256;    // embedding columns staged per pass
+constexpr int kRowPad = kRChunk + 8;  // bf16 per staged row: 528 B (33 x 16 B), keeps ldmatrix conflict-free
 constexpr int kMaxT = 32;
 
 struct SmemWalk {
@@ -35,6 +35,17 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(addr));
+}
+
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
+               "l"(gmem_src)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -63,13 +74,13 @@ __device__ void tile_bf16(const __nv_bfloat16* __restrict__ U, const __nv_bfloat
     const int rc = min(kRChunk, R - r0);  // multiple of 16
     const int vec_per_row = rc / 8;       // 16-byte vectors per staged row
     __syncwarp();
+    // every 16-byte piece of the 32 gathered rows is issued before any is waited for
     for (int v = lane; v < kKP * vec_per_row; v += 32) {
       const int row = v / vec_per_row, cv = v % vec_per_row;
-      const uint4 a = *reinterpret_cast<const uint4*>(U + (size_t)prev[row] * R + r0 + cv * 8);
-      const uint4 b = *reinterpret_cast<const uint4*>(V + (size_t)cur[row] * R + r0 + cv * 8);
-      *reinterpret_cast<uint4*>(stA + row * kRowPad + cv * 8) = a;
-      *reinterpret_cast<uint4*>(stB + row * kRowPad + cv * 8) = b;
+      cp_async16(stA + row * kRowPad + cv * 8, U + (size_t)prev[row] * R + r0 + cv * 8);
+      cp_async16(stB + row * kRowPad + cv * 8, V + (size_t)cur[row] * R + r0 + cv * 8);
     }
+    cp_async_wait_all();
     __syncwarp();
     for (int k0 = 0; k0 < rc; k0 += 16) {
       uint32_t a[4], b[4];
@@ -144,13 +155,10 @@ __global__ void __launch_bounds__(32 * kWarps)
   __syncthreads();
 
   for (int t = warp; t < T; t += kWarps) {
-    int32_t prev[kKP];
     const int32_t* cur = sw.ids[t];
-#pragma unroll
-    for (int i = 0; i < kKP; ++i) prev[i] = (t == 0) ? sw.anchor : sw.ids[t - 1][i];
-    // stage prev ids in shared memory as well (the bf16 path indexes them per lane)
+    // previous candidates of this boundary: the anchor for slot 0, else slot t-1's list
     __shared__ int32_t prev_s[kWarps][kKP];
-    if (lane < kKP) prev_s[warp][lane] = prev[lane];
+    if (lane < kKP) prev_s[warp][lane] = (t == 0) ? sw.anchor : sw.ids[t - 1][lane];
     __syncwarp();
     if constexpr (kBf16) {
       __nv_bfloat16* stA = stage + (size_t)warp * 2 * kKP * kRowPad;
@@ -170,24 +178,27 @@ __global__ void __launch_bounds__(32 * kWarps)
   const bool live = j < K;
   if (!greedy) {
     // Viterbi in fp32: delta_0 = lp_0 + tau_0(0, j); delta_t = lp_t + max_i (delta_{t-1}(i) + tau_t(i, j)).
+    // delta(i) is read back from shared memory by every lane (a broadcast), so the inner
+    // loop has no shuffle latency in it.
+    __shared__ float dsh[kKP];
     float delta = live ? sw.lp[0][j] + sw.tau[0][0][j] : -INFINITY;
     for (int t = 1; t < T; ++t) {
-      float best = 0.f;
-      int arg = 0;
-      for (int i = 0; i < K; ++i) {
-        const float di = __shfl_sync(0xffffffffu, delta, i);
-        if (live) {
-          const float v = di + sw.tau[t][i][j];
-          if (i == 0 || v > best) {
+      if (lane < kKP) dsh[lane] = delta;
+      __syncwarp();
+      if (live) {
+        float best = dsh[0] + sw.tau[t][0][j];
+        int arg = 0;
+        for (int i = 1; i < K; ++i) {
+          const float v = dsh[i] + sw.tau[t][i][j];
+          if (v > best) {
             best = v;
             arg = i;
           }
         }
-      }
-      if (live) {
         delta = sw.lp[t][j] + best;
         sw.bp[t][j] = (int8_t)arg;
       }
+      __syncwarp();
     }
     // arg-max over lanes, lowest index on ties
     float bv = delta;
