@@ -167,19 +167,21 @@ def tail_roofline_us(sh, M, bw_gbs, tflops):
     return max(flop / (tflops * 1e12), sh.vocab * sh.hidden * 2 / (bw_gbs * 1e9)) * 1e6
 
 
-def traffic_record(kind: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current
-    kernel source (hash match); otherwise None."""
+def traffic_record(M: int):
+    """DRAM bytes per launch of the LM-head kernel from the committed ncu summary, if it was
+    taken on the current kernel source (hash match) and for this row count; otherwise None."""
+    import re
     try:
-        with open(os.path.join(ROOT, "profiles", "lmhead_traffic.json")) as f:
-            rec = json.load(f)
+        text = open(os.path.join(ROOT, "profiles", "lmhead_topk_b1_page.md")).read()
         src = os.path.join(ROOT, "block_drafter_dflash2_gb300", "csrc")
         h = hashlib.sha256()
         for name in ("tc_gemm.cuh", "ptx.cuh", "lmhead_tc.cu"):
             h.update(open(os.path.join(src, name), "rb").read())
-        if rec.get("source_sha256") != h.hexdigest():
+        m_hash = re.search(r"^source_sha256: (\w+)", text, re.M)
+        m_traffic = re.search(rf"^traffic_bytes_full_launch_M{M}: (\d+)", text, re.M)
+        if not m_hash or m_hash.group(1) != h.hexdigest() or not m_traffic:
             return None
-        return rec.get(kind)
+        return int(m_traffic.group(1))
     except Exception:
         return None
 
@@ -373,7 +375,7 @@ def run_ours(args, rank, world, local_rank):
                       "merge": round(statistics.mean(merge_ms) * 1e3, 2),
                       "transition_walk": round(statistics.mean(walk_ms) * 1e3, 2)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": bw, "unit": "GB/s",
-                     "frac": round(achieved / bw, 4), "traffic": traffic_record(f"M={M}"),
+                     "frac": round(achieved / bw, 4), "traffic": traffic_record(M),
                      "kernel": "tc_gemm_kernel<EpiTopK> (LM-head contraction + fused top-16/lse)",
                      "peak_source": f"{peak_kind} hbm_gbs"},
         "e2e": {"value": round(e2e_val, 2), "unit": UNIT,

@@ -68,6 +68,7 @@ struct Plan {
   int lm_parts;
   int conv_parts;
   int chain_grid;  // > 0: all conv layers in one cooperative launch of this many CTAs
+  int chain_taps;  // the most projection rows one of its CTAs owns
   bool raw, greedy;
 };
 
@@ -109,13 +110,15 @@ dflash2_status_t make_plan(const dflash2_shape_t* s, Plan& p) {
     p.conv_parts = per < p_units ? per : p_units;
     const int groups = p.H / 16;
     const int grid = sms < groups ? sms : groups;
-    p.chain_grid = (p.M <= 64 && (groups + grid - 1) / grid <= 4) ? grid : 0;
+    p.chain_taps = 2 * ((groups + grid - 1) / grid);
+    p.chain_grid = df::conv_chain_small_fits(p.M, p.H, p.chain_taps) ? grid : 0;
   } else {
     p.n_rc = 1;
     p.a_tail_rows = 0;
     p.lm_parts = sms < v_units ? sms : v_units;
     p.conv_parts = 0;
     p.chain_grid = 0;
+    p.chain_taps = 0;
   }
   if (p.lm_parts > 1024) p.lm_parts = 1024;
   return DFLASH2_OK;
@@ -177,7 +180,7 @@ dflash2_status_t run_conv(const Plan& p, const void* x, const void* conv_w, void
   if (p.NL == 0) return cuda_status(cudaMemcpyAsync(y, x, act, cudaMemcpyDeviceToDevice, s));
   if (p.bf16 && p.chain_grid > 0)
     return cuda_status(df::launch_conv_chain_small(x, conv_w, w.conv0, w.conv1, y, p.M, p.H, p.T, p.NL,
-                                                   p.raw ? 1 : 0, w.bar, w.err, p.chain_grid, s));
+                                                   p.raw ? 1 : 0, p.chain_taps, w.bar, w.err, p.chain_grid, s));
   const void* cur = x;
   for (int l = 0; l < p.NL; ++l) {
     void* out = (l == p.NL - 1) ? y : ((l % 2 == 0) ? w.conv0 : w.conv1);
@@ -333,9 +336,14 @@ dflash2_status_t dflash2_draft_tail(const dflash2_shape_t* shape, const void* hi
     if ((st = run_conv(p, hidden, conv_w, zbuf, w, s)) != DFLASH2_OK) return st;
     z = zbuf;
   }
+  if ((st = run_partials(p, z, lm_head, w, s)) != DFLASH2_OK) return st;
+  if (df::select_walk_smem(p.lm_parts) <= 227 * 1024)  // merge fused with the walk
+    return cuda_status(df::launch_select_walk(p.bf16, w.part_val, w.part_id, w.part_ms, p.lm_parts, p.M, anchor, U,
+                                              V, p.B, p.T, p.K, p.R, p.V, p.greedy ? 1 : 0, cand_ids, cand_lp, lse,
+                                              path_ids, path_idx, score, w.err, s));
   int32_t* ids = cand_ids ? cand_ids : w.cand_ids;
   float* lp = cand_lp ? cand_lp : w.cand_lp;
-  if ((st = run_topk(p, z, lm_head, ids, lp, lse, w, s)) != DFLASH2_OK) return st;
+  if ((st = run_merge(p, ids, lp, lse, w, s)) != DFLASH2_OK) return st;
   return run_walk(p, anchor, ids, lp, U, V, path_ids, path_idx, score, w, s);
 }
 

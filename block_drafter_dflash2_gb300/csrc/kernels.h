@@ -23,10 +23,11 @@ cudaError_t launch_conv_layer_bf16(const CUtensorMap& a, const CUtensorMap& a_ta
 
 // All conv layers in one cooperative launch for M <= 64 rows (bf16); `grid` CTAs, each owning
 // a contiguous range of at most 4 channel groups. Zeroes *bar_count on the stream first.
-size_t conv_chain_small_smem(int H);
+// `wtaps` = the most projection rows any CTA owns (2 * ceil(groups / grid)).
+bool conv_chain_small_fits(int M, int H, int wtaps);
 cudaError_t launch_conv_chain_small(const void* x, const void* conv_w, void* buf0, void* buf1, void* z, int M,
-                                    int H, int T, int NL, int raw, unsigned* bar_count, int32_t* err, int grid,
-                                    cudaStream_t s);
+                                    int H, int T, int NL, int raw, int wtaps, unsigned* bar_count, int32_t* err,
+                                    int grid, cudaStream_t s);
 
 // fp32 instantiations (small sizes).
 cudaError_t launch_conv_layer_f32(const float* x, const float* w, float* y, int M, int H, int T, int raw,
@@ -37,6 +38,15 @@ cudaError_t launch_lmhead_topk_f32(const float* z, const float* w, const TcGemmA
 // Merge of the per-partition top-16 lists and (max, sum) pairs -> top-K, log-probs, lse.
 cudaError_t launch_topk_merge(const float* part_val, const int32_t* part_id, const float* part_ms, int parts,
                               int M, int K, int32_t* cand_ids, float* cand_lp, float* lse, cudaStream_t s);
+
+// Merge of the partials fused with the transition tiles and the walk, one CTA per sequence
+// (the whole-tail call); cand_ids / cand_lp / lse may be null. Needs select_walk_smem(parts)
+// bytes of shared memory (at most 227 KB).
+size_t select_walk_smem(int parts);
+cudaError_t launch_select_walk(bool bf16, const float* part_val, const int32_t* part_id, const float* part_ms,
+                               int parts, int M, const int32_t* anchor, const void* U, const void* V, int B, int T,
+                               int K, int R, int vocab, int greedy, int32_t* cand_ids, float* cand_lp, float* lse,
+                               int32_t* path_ids, int32_t* path_idx, float* score, int32_t* err, cudaStream_t s);
 
 // Transition tiles + Viterbi / greedy walk, one CTA per sequence.
 cudaError_t launch_transition_walk(bool bf16, const int32_t* anchor, const int32_t* cand_ids,

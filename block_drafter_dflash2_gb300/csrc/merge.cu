@@ -10,29 +10,13 @@
 #include <math.h>
 
 #include "kernels.h"
+#include "select.cuh"
 
 namespace df {
 
 namespace {
 constexpr int kThreads = 128;
 constexpr int kMaxParts = 1024;
-
-__device__ __forceinline__ bool better(float v, int32_t id, float bv, int32_t bid) {
-  return v > bv || (v == bv && id < bid);
-}
-
-// Unsigned key with the same order as the float (negative values reversed); 0 = no entry.
-__device__ __forceinline__ uint32_t order_key(float v) {
-  const uint32_t u = __float_as_uint(v);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
-                   static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
-               "l"(gmem_src)
-               : "memory");
-}
 
 __global__ void __launch_bounds__(kThreads)
     topk_merge_kernel(const float4* __restrict__ part_val, const int4* __restrict__ part_id,
@@ -53,7 +37,7 @@ __global__ void __launch_bounds__(kThreads)
     cp_async16(reinterpret_cast<float4*>(sv) + e, part_val + src);
     cp_async16(reinterpret_cast<int4*>(si) + e, part_id + src);
   }
-  asm volatile("cp.async.commit_group;" ::: "memory");
+  cp_async_commit();
   for (int p = tid; p < parts; p += kThreads) head[p] = 0;
 
   float m = -INFINITY;
@@ -80,47 +64,15 @@ __global__ void __launch_bounds__(kThreads)
     lse_s = m + logf(t);
     if (lse_out) lse_out[row] = lse_s;
   }
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  cp_async_wait_all();
   __syncthreads();
   if (warp != 0) return;
   const float lse = lse_s;
 
-  auto rescan = [&](float& bv, int32_t& bid, int& bp) {
-    bv = -INFINITY;
-    bid = 0x7fffffff;
-    bp = -1;
-    for (int p = lane; p < parts; p += 32) {
-      const int h = head[p];
-      if (h < 16) {
-        const float v = sv[p * 16 + h];
-        const int32_t id = si[p * 16 + h];
-        if (bp < 0 || better(v, id, bv, bid)) {
-          bv = v;
-          bid = id;
-          bp = p;
-        }
-      }
-    }
-  };
-  float bv;
-  int32_t bid;
-  int bp;
-  rescan(bv, bid, bp);
-  for (int k = 0; k < K; ++k) {
-    const uint32_t key = bp >= 0 ? order_key(bv) : 0u;
-    const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
-    const bool tied = key == kmax && bp >= 0;
-    const uint32_t wid = __reduce_min_sync(0xffffffffu, tied ? (uint32_t)bid : 0xffffffffu);
-    const uint32_t win = __ballot_sync(0xffffffffu, tied && (uint32_t)bid == wid);  // ids are unique
-    const int wl = __ffs(win) - 1;
-    if (lane == wl) {
-      cand_ids[(size_t)row * K + k] = bid;
-      cand_lp[(size_t)row * K + k] = bv - lse;
-      head[bp] += 1;
-      rescan(bv, bid, bp);
-    }
-    __syncwarp();
-  }
+  warp_merge_lists(sv, si, head, parts, K, [&](int k, int32_t id, float v) {
+    cand_ids[(size_t)row * K + k] = id;
+    cand_lp[(size_t)row * K + k] = v - lse;
+  });
 }
 }  // namespace
 

@@ -1,4 +1,5 @@
-// Transition tiles and the walk from the anchor, one CTA (8 warps) per sequence.
+// Transition tiles and the walk from the anchor, one CTA (8 warps) per sequence; and the
+// same walk fused with the top-K merge for the whole-tail call.
 //
 // For slot boundary t the previous candidates are the anchor (t = 0, repeated K times) or
 // slot t-1's candidates; the current ones are slot t's. Warp t % 8 gathers the 16 U-rows
@@ -9,10 +10,16 @@
 // for every j, the max over i of delta(i) + tau(i, j) with the lowest i on ties, adds
 // lp_t(j), and keeps the back-pointer; a shuffle arg-max (lowest index on ties) picks the
 // final state and lane 0 reads the path back.
+//
+// The fused kernel first merges the sequence's T rows (warp t % 8 takes row t): the row's
+// per-partition top-16 lists and (max, sum) pairs are staged with cp.async, lse is reduced
+// across the warp and the K best candidates are picked by the warp-wide merge; they stay in
+// shared memory for the walk (and are also written out).
 #include <cuda_bf16.h>
 
 #include "../../include/dflash2.h"
 #include "kernels.h"
+#include "select.cuh"
 
 namespace df {
 
@@ -35,17 +42,6 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(addr));
-}
-
-__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
-                   static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
-               "l"(gmem_src)
-               : "memory");
-}
-
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -80,6 +76,7 @@ __device__ void tile_bf16(const __nv_bfloat16* __restrict__ U, const __nv_bfloat
       cp_async16(stA + row * kRowPad + cv * 8, U + (size_t)prev[row] * R + r0 + cv * 8);
       cp_async16(stB + row * kRowPad + cv * 8, V + (size_t)cur[row] * R + r0 + cv * 8);
     }
+    cp_async_commit();
     cp_async_wait_all();
     __syncwarp();
     for (int k0 = 0; k0 < rc; k0 += 16) {
@@ -122,42 +119,26 @@ __device__ void tile_f32(const float* __restrict__ U, const float* __restrict__ 
   }
 }
 
-template <bool kBf16>
-__global__ void __launch_bounds__(32 * kWarps)
-    transition_walk_kernel(const int32_t* __restrict__ anchor, const int32_t* __restrict__ cand_ids,
-                           const float* __restrict__ cand_lp, const void* __restrict__ Uv,
-                           const void* __restrict__ Vv, int T, int K, int R, int vocab, int greedy,
-                           int32_t* __restrict__ path_ids, int32_t* __restrict__ path_idx, float* __restrict__ score,
-                           int32_t* err) {
-  extern __shared__ __align__(16) uint8_t smem_raw[];
-  SmemWalk& sw = *reinterpret_cast<SmemWalk*>(smem_raw);
-  __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(smem_raw + ((sizeof(SmemWalk) + 127) & ~size_t(127)));
-  const int b = blockIdx.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  if (threadIdx.x == 0) sw.anchor = clamp_id(anchor[b], vocab, err, DFLASH2_DEVERR_ANCHOR_RANGE);
+// Pads candidate slots K..15 of every slot with a valid id and -inf score (call after the
+// real candidates are in sw, then __syncthreads).
+__device__ void pad_candidates(SmemWalk& sw, int T, int K) {
   for (int e = threadIdx.x; e < T * kKP; e += blockDim.x) {
-    const int t = e / kKP, j = e % kKP;
-    if (j < K) {
-      const size_t at = ((size_t)b * T + t) * K + j;
-      sw.ids[t][j] = clamp_id(cand_ids[at], vocab, err, DFLASH2_DEVERR_CANDIDATE_RANGE);
-      sw.lp[t][j] = cand_lp[at];
-    }
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < T * kKP; e += blockDim.x) {  // pad slots K..15 with a valid id
     const int t = e / kKP, j = e % kKP;
     if (j >= K) {
       sw.ids[t][j] = sw.ids[t][0];
       sw.lp[t][j] = -INFINITY;
     }
   }
-  __syncthreads();
+}
 
+// All T transition tiles of one sequence; warp w builds the tiles t = w, w + 8, ...
+template <bool kBf16>
+__device__ void build_tiles(SmemWalk& sw, int T, int R, const void* Uv, const void* Vv, __nv_bfloat16* stage) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ int32_t prev_s[kWarps][kKP];
   for (int t = warp; t < T; t += kWarps) {
     const int32_t* cur = sw.ids[t];
     // previous candidates of this boundary: the anchor for slot 0, else slot t-1's list
-    __shared__ int32_t prev_s[kWarps][kKP];
     if (lane < kKP) prev_s[warp][lane] = (t == 0) ? sw.anchor : sw.ids[t - 1][lane];
     __syncwarp();
     if constexpr (kBf16) {
@@ -171,9 +152,12 @@ __global__ void __launch_bounds__(32 * kWarps)
     }
     __syncwarp();
   }
-  __syncthreads();
+}
 
-  if (warp != 0) return;
+// The walk for sequence b on warp 0 (the other warps return before calling it).
+__device__ void walk_warp0(SmemWalk& sw, int b, int T, int K, int greedy, int32_t* __restrict__ path_ids,
+                           int32_t* __restrict__ path_idx, float* __restrict__ score) {
+  const int lane = threadIdx.x & 31;
   const int j = lane;
   const bool live = j < K;
   if (!greedy) {
@@ -247,7 +231,142 @@ __global__ void __launch_bounds__(32 * kWarps)
     }
   }
 }
+
+template <bool kBf16>
+__global__ void __launch_bounds__(32 * kWarps)
+    transition_walk_kernel(const int32_t* __restrict__ anchor, const int32_t* __restrict__ cand_ids,
+                           const float* __restrict__ cand_lp, const void* __restrict__ Uv,
+                           const void* __restrict__ Vv, int T, int K, int R, int vocab, int greedy,
+                           int32_t* __restrict__ path_ids, int32_t* __restrict__ path_idx, float* __restrict__ score,
+                           int32_t* err) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  SmemWalk& sw = *reinterpret_cast<SmemWalk*>(smem_raw);
+  __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(smem_raw + ((sizeof(SmemWalk) + 127) & ~size_t(127)));
+  const int b = blockIdx.x;
+
+  if (threadIdx.x == 0) sw.anchor = clamp_id(anchor[b], vocab, err, DFLASH2_DEVERR_ANCHOR_RANGE);
+  for (int e = threadIdx.x; e < T * kKP; e += blockDim.x) {
+    const int t = e / kKP, j = e % kKP;
+    if (j < K) {
+      const size_t at = ((size_t)b * T + t) * K + j;
+      sw.ids[t][j] = clamp_id(cand_ids[at], vocab, err, DFLASH2_DEVERR_CANDIDATE_RANGE);
+      sw.lp[t][j] = cand_lp[at];
+    }
+  }
+  __syncthreads();
+  pad_candidates(sw, T, K);
+  __syncthreads();
+  build_tiles<kBf16>(sw, T, R, Uv, Vv, stage);
+  __syncthreads();
+  if ((threadIdx.x >> 5) != 0) return;
+  walk_warp0(sw, b, T, K, greedy, path_ids, path_idx, score);
+}
+
+// Bytes of one warp's merge staging: values and ids [parts][16], (max, sum) [parts], heads.
+__host__ __device__ inline size_t merge_stage_bytes(int parts) {
+  return (((size_t)parts * 16 * 8 + (size_t)parts * 8 + (size_t)parts) + 127) & ~size_t(127);
+}
+
+template <bool kBf16>
+__global__ void __launch_bounds__(32 * kWarps)
+    select_walk_kernel(const float* __restrict__ part_val, const int32_t* __restrict__ part_id,
+                       const float2* __restrict__ part_ms, int parts, int M, const int32_t* __restrict__ anchor,
+                       const void* __restrict__ Uv, const void* __restrict__ Vv, int T, int K, int R, int vocab,
+                       int greedy, int32_t* __restrict__ cand_ids, float* __restrict__ cand_lp,
+                       float* __restrict__ lse_out, int32_t* __restrict__ path_ids, int32_t* __restrict__ path_idx,
+                       float* __restrict__ score, int32_t* err) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  SmemWalk& sw = *reinterpret_cast<SmemWalk*>(smem_raw);
+  uint8_t* region = smem_raw + ((sizeof(SmemWalk) + 127) & ~size_t(127));
+  const int b = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) sw.anchor = clamp_id(anchor[b], vocab, err, DFLASH2_DEVERR_ANCHOR_RANGE);
+  {
+    const size_t wbytes = merge_stage_bytes(parts);
+    float* sv = reinterpret_cast<float*>(region + warp * wbytes);
+    int32_t* si = reinterpret_cast<int32_t*>(sv + parts * 16);
+    float2* sms = reinterpret_cast<float2*>(si + parts * 16);
+    uint8_t* head = reinterpret_cast<uint8_t*>(sms + parts);
+    for (int t = warp; t < T; t += kWarps) {
+      const int row = b * T + t;
+      for (int e = lane; e < parts * 4; e += 32) {
+        const int p = e >> 2, q = e & 3;
+        const size_t src = ((size_t)p * M + row) * 16 + q * 4;
+        cp_async16(sv + e * 4, part_val + src);
+        cp_async16(si + e * 4, part_id + src);
+      }
+      cp_async_commit();
+      for (int p = lane; p < parts; p += 32) {
+        sms[p] = part_ms[(size_t)p * M + row];
+        head[p] = 0;
+      }
+      float m = -INFINITY;
+      for (int p = lane; p < parts; p += 32) m = fmaxf(m, sms[p].x);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      float s = 0.f;
+      for (int p = lane; p < parts; p += 32)
+        if (sms[p].y > 0.f) s += sms[p].y * expf(sms[p].x - m);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      const float lse = m + logf(s);
+      if (lane == 0 && lse_out) lse_out[row] = lse;
+      cp_async_wait_all();
+      __syncwarp();
+      warp_merge_lists(sv, si, head, parts, K, [&](int k, int32_t id, float v) {
+        const float lp = v - lse;
+        sw.ids[t][k] = id;
+        sw.lp[t][k] = lp;
+        if (cand_ids) cand_ids[(size_t)row * K + k] = id;
+        if (cand_lp) cand_lp[(size_t)row * K + k] = lp;
+      });
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  pad_candidates(sw, T, K);
+  __syncthreads();
+  build_tiles<kBf16>(sw, T, R, Uv, Vv, reinterpret_cast<__nv_bfloat16*>(region));
+  __syncthreads();
+  if (warp != 0) return;
+  walk_warp0(sw, b, T, K, greedy, path_ids, path_idx, score);
+}
+
+constexpr size_t kWalkStageBytes = (size_t)kWarps * 2 * kKP * kRowPad * sizeof(__nv_bfloat16);
+
 }  // namespace
+
+size_t select_walk_smem(int parts) {
+  const size_t base = (sizeof(SmemWalk) + 127) & ~size_t(127);
+  const size_t merge = (size_t)kWarps * merge_stage_bytes(parts);
+  return base + (merge > kWalkStageBytes ? merge : kWalkStageBytes);
+}
+
+cudaError_t launch_select_walk(bool bf16, const float* part_val, const int32_t* part_id, const float* part_ms,
+                               int parts, int M, const int32_t* anchor, const void* U, const void* V, int B, int T,
+                               int K, int R, int vocab, int greedy, int32_t* cand_ids, float* cand_lp, float* lse,
+                               int32_t* path_ids, int32_t* path_idx, float* score, int32_t* err, cudaStream_t s) {
+  if (T > kMaxT || K > kKP) return cudaErrorInvalidValue;
+  const size_t smem = select_walk_smem(parts);
+  if (smem > 227 * 1024) return cudaErrorInvalidValue;
+  cudaError_t e;
+  const float2* ms = reinterpret_cast<const float2*>(part_ms);
+  if (bf16) {
+    e = cudaFuncSetAttribute(select_walk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    select_walk_kernel<true><<<B, 32 * kWarps, smem, s>>>(part_val, part_id, ms, parts, M, anchor, U, V, T, K, R,
+                                                           vocab, greedy, cand_ids, cand_lp, lse, path_ids,
+                                                           path_idx, score, err);
+  } else {
+    e = cudaFuncSetAttribute(select_walk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    select_walk_kernel<false><<<B, 32 * kWarps, smem, s>>>(part_val, part_id, ms, parts, M, anchor, U, V, T, K, R,
+                                                            vocab, greedy, cand_ids, cand_lp, lse, path_ids,
+                                                            path_idx, score, err);
+  }
+  return cudaGetLastError();
+}
 
 cudaError_t launch_transition_walk(bool bf16, const int32_t* anchor, const int32_t* cand_ids,
                                    const float* cand_lp, const void* U, const void* V, int B, int T, int K,
@@ -255,7 +374,7 @@ cudaError_t launch_transition_walk(bool bf16, const int32_t* anchor, const int32
                                    float* score, int32_t* err, cudaStream_t s) {
   if (T > kMaxT || K > kKP) return cudaErrorInvalidValue;
   const size_t base = (sizeof(SmemWalk) + 127) & ~size_t(127);
-  const size_t smem = base + (bf16 ? (size_t)kWarps * 2 * kKP * kRowPad * sizeof(__nv_bfloat16) : 0);
+  const size_t smem = base + (bf16 ? kWalkStageBytes : 0);
   cudaError_t e;
   if (bf16) {
     e = cudaFuncSetAttribute(transition_walk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
