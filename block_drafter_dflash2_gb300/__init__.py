@@ -85,6 +85,8 @@ def load(path: str = LIB_PATH):
     lib.dflash2_conv.restype = st
     lib.dflash2_select_topk.argtypes = [sp, vp, vp, i32p, vp, vp, vp, sz, vp]
     lib.dflash2_select_topk.restype = st
+    lib.dflash2_select_topk_noalloc.argtypes = [sp, vp, vp, i32p, vp, vp, vp]
+    lib.dflash2_select_topk_noalloc.restype = st
     lib.dflash2_lmhead_partials.argtypes = [sp, vp, vp, vp, sz, vp]
     lib.dflash2_lmhead_partials.restype = st
     lib.dflash2_merge_partials.argtypes = [sp, i32p, vp, vp, vp, sz, vp]
@@ -163,6 +165,15 @@ def select_topk(shape: Shape, rows, lm_head, cand_ids, cand_lp, lse, ws, stream=
     wp, wn = _ws(ws)
     _check(load().dflash2_select_topk(ctypes.byref(shape), _ptr(rows), _ptr(lm_head), _ptr(cand_ids),
                                       _ptr(cand_lp), _ptr(lse), wp, wn, _stream(stream)), "dflash2_select_topk")
+
+
+def select_topk_noalloc(shape: Shape, rows, lm_head, cand_ids, cand_lp, lse, stream=None):
+    """dflash2_select_topk_noalloc: the same selection with the library's own fixed device
+    scratch instead of a workspace, for callers that cannot allocate device memory. Calls
+    share that scratch, so calls that may overlap on the GPU must be serialised."""
+    _check(load().dflash2_select_topk_noalloc(ctypes.byref(shape), _ptr(rows), _ptr(lm_head), _ptr(cand_ids),
+                                              _ptr(cand_lp), _ptr(lse), _stream(stream)),
+           "dflash2_select_topk_noalloc")
 
 
 def lmhead_partials(shape: Shape, rows, lm_head, ws, stream=None):

@@ -239,6 +239,51 @@ dflash2_status_t run_walk(const Plan& p, const int32_t* anchor, const int32_t* i
                                                 p.greedy ? 1 : 0, path_ids, path_idx, score, w.err, s));
 }
 
+// ---- scratch for dflash2_select_topk_noalloc: a fixed device array instead of a caller
+// workspace. Every device that loads the library holds it until the process exits. Host
+// code sees only a host-side stand-in for the symbol; its device address is looked up once
+// per device with cudaGetSymbolAddress, with that device current.
+constexpr size_t kStaticScratchBytes = 4u << 20;  // 4 MiB
+
+std::mutex g_scratch_mu;
+void* g_scratch_dev[kMaxDevices];
+
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_select_scratch[kStaticScratchBytes];
+
+namespace {
+
+dflash2_status_t static_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DFLASH2_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_dev[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_select_scratch) != cudaSuccess || ptr == nullptr) return DFLASH2_ERR_CUDA;
+    g_scratch_dev[dev] = ptr;
+  }
+  *out = g_scratch_dev[dev];
+  return DFLASH2_OK;
+}
+
+// The part of the workspace layout that the top-K selection uses: error word and partials.
+Ws carve_select(const Plan& p, void* base) {
+  Ws w{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    void* q = base ? static_cast<char*>(base) + off : nullptr;
+    off += up256(bytes);
+    return q;
+  };
+  w.err = static_cast<int32_t*>(take(256));
+  w.part_val = static_cast<float*>(take((size_t)p.lm_parts * p.M * 16 * 4));
+  w.part_id = static_cast<int32_t*>(take((size_t)p.lm_parts * p.M * 16 * 4));
+  w.part_ms = static_cast<float*>(take((size_t)p.lm_parts * p.M * 2 * 4));
+  w.total = off;
+  return w;
+}
+
 }  // namespace
 
 extern "C" {
@@ -272,6 +317,24 @@ dflash2_status_t dflash2_select_topk(const dflash2_shape_t* shape, const void* r
   Ws w;
   if ((st = check_ws(p, ws, ws_bytes, w)) != DFLASH2_OK) return st;
   return run_topk(p, rows, lm_head, cand_ids, cand_lp, lse, w, static_cast<cudaStream_t>(stream));
+}
+
+dflash2_status_t dflash2_select_topk_noalloc(const dflash2_shape_t* shape, const void* rows, const void* lm_head,
+                                             int32_t* cand_ids, float* cand_lp, float* lse, void* stream) {
+  Plan p;
+  dflash2_status_t st = make_plan(shape, p);
+  if (st != DFLASH2_OK) return st;
+  if (!rows || !lm_head || !cand_ids || !cand_lp) return DFLASH2_ERR_INVALID_ARGUMENT;
+  if (!aligned16(rows) || !aligned16(lm_head)) return DFLASH2_ERR_INVALID_ARGUMENT;
+  if (carve_select(p, nullptr).total > kStaticScratchBytes) return DFLASH2_ERR_WORKSPACE_TOO_SMALL;
+  void* scratch = nullptr;
+  if ((st = static_scratch(&scratch)) != DFLASH2_OK) return st;
+  const Ws w = carve_select(p, scratch);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the error word must start at zero; the partials are overwritten in full by every call
+  if (cudaMemsetAsync(w.err, 0, sizeof(int32_t), s) != cudaSuccess) return DFLASH2_ERR_CUDA;
+  if ((st = run_partials(p, rows, lm_head, w, s)) != DFLASH2_OK) return st;
+  return run_merge(p, cand_ids, cand_lp, lse, w, s);
 }
 
 dflash2_status_t dflash2_lmhead_partials(const dflash2_shape_t* shape, const void* rows, const void* lm_head,

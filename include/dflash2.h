@@ -116,6 +116,27 @@ dflash2_status_t dflash2_select_topk(const dflash2_shape_t* shape, const void* r
                                      int32_t* cand_ids, float* cand_lp, float* lse,
                                      void* ws, size_t ws_bytes, void* stream);
 
+/* dflash2_select_topk without a workspace argument and without any allocation, for callers
+ * that cannot obtain device memory at the point of the call: a plugin inside a serving
+ * engine that has already reserved the whole GPU for its own pools and exposes no
+ * allocator, code that runs while a CUDA graph is being captured (where cudaMalloc is not
+ * allowed), or a latency-critical loop that must not risk the implicit device
+ * synchronisation an allocation can cause. No counterpart in the DFlash2 pages: it is the
+ * same selection as dflash2_select_topk (same kernels, same results), with its scratch in a
+ * fixed 4 MiB device array inside the library instead of the caller's workspace.
+ *  - Every GPU that loads the library holds those 4 MiB until the process exits.
+ *  - The first call on each device looks up the array's device address (with that device
+ *    current); make that first call before any stream capture that includes this call.
+ *  - Shapes whose partials need more than 4 MiB (parts * rows * 136 bytes + 256, where
+ *    parts is about the SM count divided by ceil(rows / 128)) return
+ *    DFLASH2_ERR_WORKSPACE_TOO_SMALL before any launch.
+ *  - All calls share the array: calls that may overlap on the GPU (different streams, or
+ *    different host threads) race with each other and must be serialised by the caller.
+ *  - Each call clears the array's error word first; device-side errors of this call are
+ *    not reported (there is no workspace to read them from). */
+dflash2_status_t dflash2_select_topk_noalloc(const dflash2_shape_t* shape, const void* rows, const void* lm_head,
+                                             int32_t* cand_ids, float* cand_lp, float* lse, void* stream);
+
 /* The two stages of dflash2_select_topk, callable on their own (e.g. to time the
  * contraction, or to merge partials that the caller gathered from several vocab shards).
  * dflash2_lmhead_partials runs the LM-head contraction with its fused epilogue and leaves,
