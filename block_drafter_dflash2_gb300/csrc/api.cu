@@ -17,6 +17,7 @@ using df::TcGemmArgs;
 constexpr int kMaxDevices = 64;
 
 int g_sm_count[kMaxDevices];
+int g_clusters[kMaxDevices][9];  // resident LM-head clusters per cluster size (0 = not queried, -1 = none)
 std::once_flag g_encode_once;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -29,6 +30,17 @@ int sm_count() {
     g_sm_count[dev] = n;
   }
   return g_sm_count[dev];
+}
+
+// Resident clusters of `cluster` LM-head CTAs on the current device, cached.
+int max_clusters(int cluster) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices || cluster > 8) return 0;
+  if (g_clusters[dev][cluster] == 0) {
+    const int n = df::lmhead_max_active_clusters(cluster);
+    g_clusters[dev][cluster] = n > 0 ? n : -1;
+  }
+  return g_clusters[dev][cluster] > 0 ? g_clusters[dev][cluster] : 0;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
@@ -64,6 +76,7 @@ struct Plan {
   bool bf16;
   size_t esz;
   int n_rc;
+  int lm_cluster;   // CTAs per cluster in the LM-head contraction (1 = no clusters)
   int a_tail_rows;  // rows of the last 128-row chunk, rounded up to 8
   int lm_parts;
   int conv_parts;
@@ -107,6 +120,16 @@ dflash2_status_t make_plan(const dflash2_shape_t* s, Plan& p) {
     p.a_tail_rows = (p.M % 128 == 0) ? 128 : ((p.M % 128 + 7) / 8) * 8;
     const int per = sms / p.n_rc > 0 ? sms / p.n_rc : 1;
     p.lm_parts = per < v_units ? per : v_units;
+    p.lm_cluster = 1;
+    if (p.n_rc == 2 || p.n_rc == 4 || p.n_rc == 8) {
+      // the row chunks of a column range form a cluster and share its weight tiles; as many
+      // ranges as clusters fit on the device at once
+      const int nc = max_clusters(p.n_rc);
+      if (nc > 0) {
+        p.lm_cluster = p.n_rc;
+        p.lm_parts = nc < v_units ? nc : v_units;
+      }
+    }
     p.conv_parts = per < p_units ? per : p_units;
     const int groups = p.H / 16;
     const int grid = sms < groups ? sms : groups;
@@ -114,6 +137,7 @@ dflash2_status_t make_plan(const dflash2_shape_t* s, Plan& p) {
     p.chain_grid = df::conv_chain_small_fits(p.M, p.H, p.chain_taps) ? grid : 0;
   } else {
     p.n_rc = 1;
+    p.lm_cluster = 1;
     p.a_tail_rows = 0;
     p.lm_parts = sms < v_units ? sms : v_units;
     p.conv_parts = 0;
@@ -190,7 +214,7 @@ dflash2_status_t run_conv(const Plan& p, const void* x, const void* conv_w, void
       if (!encode_bf16_2d(&ma, cur, p.H, p.M, 128) || !encode_bf16_2d(&mat, cur, p.H, p.M, p.a_tail_rows) ||
           !encode_bf16_2d(&mb128, wl, p.H, p.P, 128) || !encode_bf16_2d(&mb16, wl, p.H, p.P, 16))
         return DFLASH2_ERR_CUDA;
-      TcGemmArgs a{p.M, p.H, p.P, p.n_rc, p.conv_parts, p.a_tail_rows, w.err};
+      TcGemmArgs a{p.M, p.H, p.P, p.n_rc, p.conv_parts, p.a_tail_rows, 8, 1, w.err};
       if (df::launch_conv_layer_bf16(ma, mat, mb128, mb16, a, cur, out, p.T, p.raw ? 1 : 0, s) != cudaSuccess)
         return DFLASH2_ERR_CUDA;
     } else {
@@ -204,7 +228,8 @@ dflash2_status_t run_conv(const Plan& p, const void* x, const void* conv_w, void
 }
 
 dflash2_status_t run_partials(const Plan& p, const void* rows, const void* lm_head, const Ws& w, cudaStream_t s) {
-  TcGemmArgs a{p.M, p.H, p.V, p.n_rc, p.lm_parts, p.a_tail_rows, w.err};
+  // several row chunks share each column range: 256-column tiles halve the row-tile re-reads
+  TcGemmArgs a{p.M, p.H, p.V, p.n_rc, p.lm_parts, p.a_tail_rows, p.n_rc > 1 ? 16 : 8, p.lm_cluster, w.err};
   if (p.bf16) {
     CUtensorMap ma, mat, mb128, mb16;
     if (!encode_bf16_2d(&ma, rows, p.H, p.M, 128) || !encode_bf16_2d(&mat, rows, p.H, p.M, p.a_tail_rows) ||

@@ -7,8 +7,9 @@
 //
 // Work split: CTA c takes row chunk c % n_rc (128 rows) and column partition c / n_rc of
 // `parts` contiguous ranges (in units of 16 columns, balanced to one unit). A range is walked
-// in tiles of up to 128 columns; the last tile of a range is narrower (16..112 columns) and
-// is fetched in 16-row TMA boxes, so no column outside the range is ever loaded.
+// in tiles of `tile_units` units (128 or 256 columns: wider tiles re-read the row tile less
+// often when several row chunks share a column range); the last tile of a range is narrower
+// and fetched in 16-row TMA boxes, so no column outside the range is ever loaded.
 //
 // Roles (192 threads): warp 0 = TMA producer (one thread), warp 1 = MMA issuer (one thread)
 // and TMEM owner, warps 2..5 = epilogue (thread = TMEM lane = row). Shared memory holds a
@@ -16,8 +17,8 @@
 // box of the last row chunk covers only its real rows (rounded up to 8), so a small M does
 // not pay for TMA zero-fill, and the ring is cut into as many stages as fit, so small tiles
 // keep many more loads in flight. The MMA reads 128 A rows regardless; rows past the box hold
-// stale data and only feed TMEM lanes no epilogue thread reads. TMEM holds two 128-column
-// fp32 accumulators so the epilogue of tile t overlaps the MMAs of tile t+1.
+// stale data and only feed TMEM lanes no epilogue thread reads. TMEM holds two fp32
+// accumulators as wide as a tile, so the epilogue of tile t overlaps the MMAs of tile t+1.
 #pragma once
 
 #include "ptx.cuh"
@@ -27,13 +28,12 @@ namespace df {
 
 constexpr int kBK = 64;   // K per stage: one 128-byte swizzle row of bf16
 constexpr int kBM = 128;  // rows per tile (MMA M)
-constexpr int kBN = 128;  // widest tile (MMA N)
+constexpr int kBN = 128;  // widest tile with 8-unit tiles (MMA N); 16-unit tiles are 256 wide
 constexpr int kMaxStages = 48;
 constexpr int kRingBytes = 200 * 1024;           // smem ring, split into as many stages as fit
 constexpr int kASlackBytes = kBM * kBK * 2;       // the MMA always reads 128 A rows from a stage
 constexpr int kBarrierBytes = 1024;
 constexpr int kGemmThreads = 192;
-constexpr int kTmemCols = 2 * kBN;
 constexpr int kGemmSmemBytes = 1024 /*align*/ + kBarrierBytes + kRingBytes + kASlackBytes;
 
 struct TileRange {
@@ -48,14 +48,16 @@ DF_DEV TileRange tile_range(const TcGemmArgs& a, int part) {
   r.u0 = (int)((int64_t)part * units / a.parts);
   r.u1 = (int)((int64_t)(part + 1) * units / a.parts);
   r.col_end = min(r.u1 * 16, a.n_total);
-  r.num_tiles = (r.u1 - r.u0 + 7) / 8;
+  r.num_tiles = (r.u1 - r.u0 + a.tile_units - 1) / a.tile_units;
   return r;
 }
 
 // Stage geometry of one CTA: the A box is the row chunk's real rows (padded to 8; 128 for full
 // chunks), the B tile is as wide as this CTA's widest tile. Stages are as many as fit the ring.
 struct StageGeom {
-  uint32_t a_bytes, stride;
+  uint32_t a_bytes;  // bytes of this CTA's A box per stage
+  uint32_t b_off;    // offset of the B tile in a stage
+  uint32_t stride;   // bytes per stage
   int stages;
 };
 
@@ -63,8 +65,11 @@ DF_DEV StageGeom stage_geom(const TcGemmArgs& a, int rc, const TileRange& tr) {
   StageGeom g;
   const int rows = (rc == a.n_rc - 1) ? a.a_tail_rows : kBM;
   g.a_bytes = (uint32_t)rows * kBK * 2;
-  const int nmax = min(8, tr.u1 - tr.u0) * 16;
-  g.stride = (g.a_bytes + (uint32_t)nmax * kBK * 2 + 1023u) & ~1023u;
+  // CTAs of a cluster write B tiles into each other's rings: one layout for all of them
+  const uint32_t a_region = a.cluster > 1 ? (uint32_t)kBM * kBK * 2 : g.a_bytes;
+  const int nmax = min(a.tile_units, tr.u1 - tr.u0) * 16;
+  g.b_off = a_region;
+  g.stride = (a_region + (uint32_t)nmax * kBK * 2 + 1023u) & ~1023u;
   g.stages = min(kMaxStages, (int)(kRingBytes / g.stride));
   return g;
 }
@@ -94,11 +99,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const StageGeom sg = stage_geom(args, rc, tr);
   const int kblocks = args.K / kBK;
   const bool tail_chunk = (rc == args.n_rc - 1);
+  const int TU = args.tile_units;                   // tile width in 16-column units (8 or 16)
+  const uint32_t tmem_cols = (uint32_t)(2 * TU * 16);  // two accumulators: 256 or 512 columns
 
+  const int CL = args.cluster;
+  const uint16_t cl_mask = (uint16_t)((1u << CL) - 1u);
+  const int crank = CL > 1 ? (int)cluster_ctarank() : 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < sg.stages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], CL);  // released by the MMA warp of every CTA reading the stage
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -109,7 +119,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_alloc(tmem_slot, tmem_cols);
     tmem_relinquish();
   }
   if (threadIdx.x == 0) {
@@ -119,6 +129,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (CL > 1) cluster_sync();  // peers' barriers are initialised before anything lands in them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -133,8 +144,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint64_t issued = 0, issued_phase = 0;  // per-stage bits: ever issued / parity of last issue
       bool ok = true;
       for (int t = 0; t < tr.num_tiles && ok; ++t) {
-        const int cu0 = tr.u0 + t * 8;
-        const int nu = min(8, tr.u1 - cu0);
+        const int cu0 = tr.u0 + t * TU;
+        const int nu = min(TU, tr.u1 - cu0);
         const int n0 = cu0 * 16;
         const uint32_t bytes = sg.a_bytes + (uint32_t)nu * 16 * kBK * 2;
         for (int kb = 0; kb < kblocks; ++kb) {
@@ -143,14 +154,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           uint8_t* sa = ring + (size_t)stage * sg.stride;
-          uint8_t* sb = sa + sg.a_bytes;
+          uint8_t* sb = sa + sg.b_off;
           mbar_arrive_expect_tx(&full[stage], bytes);
           tma_load_2d(sa, ma, &full[stage], kb * kBK, rc * kBM, pol_a);
-          if (nu == 8) {
-            tma_load_2d(sb, &map_b128, &full[stage], kb * kBK, n0, pol_b);
+          if (CL == 1) {
+            if (nu % 8 == 0) {
+              for (int j = 0; j < nu / 8; ++j)
+                tma_load_2d(sb + j * 128 * kBK * 2, &map_b128, &full[stage], kb * kBK, n0 + 128 * j, pol_b);
+            } else {
+              for (int j = 0; j < nu; ++j)
+                tma_load_2d(sb + j * 16 * kBK * 2, &map_b16, &full[stage], kb * kBK, n0 + 16 * j, pol_b);
+            }
           } else {
-            for (int j = 0; j < nu; ++j)
-              tma_load_2d(sb + j * 16 * kBK * 2, &map_b16, &full[stage], kb * kBK, n0 + 16 * j, pol_b);
+            // this CTA's share of the B tile, multicast into every CTA of the cluster
+            const int j0 = crank * nu / CL, j1 = (crank + 1) * nu / CL;
+            for (int j = j0; j < j1;) {
+              if ((j1 - j) >= 8 && (j % 8) == 0) {
+                tma_load_2d_mc(sb + j * 16 * kBK * 2, &map_b128, &full[stage], kb * kBK, n0 + 16 * j, cl_mask,
+                               pol_b);
+                j += 8;
+              } else {
+                tma_load_2d_mc(sb + j * 16 * kBK * 2, &map_b16, &full[stage], kb * kBK, n0 + 16 * j, cl_mask,
+                               pol_b);
+                j += 1;
+              }
+            }
           }
           issued |= 1ull << stage;
           issued_phase = (issued_phase & ~(1ull << stage)) | ((uint64_t)phase << stage);
@@ -162,8 +190,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       if (!ok) {
         // Aborted: let every copy still in flight land before the CTA can exit.
+        // (one timeout ends the drain: a copy that has not landed by then is not coming)
         for (int s = 0; s < sg.stages; ++s)
-          if (issued & (1ull << s)) mbar_wait(&full[s], (uint32_t)(issued_phase >> s) & 1u, args.err, nullptr);
+          if ((issued & (1ull << s)) && !mbar_wait(&full[s], (uint32_t)(issued_phase >> s) & 1u, args.err, nullptr))
+            break;
       }
     }
   } else if (warp == 1) {
@@ -175,11 +205,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int t = 0; t < tr.num_tiles && ok; ++t) {
         const int acc = t & 1;
         const uint32_t acc_phase = (uint32_t)(t >> 1) & 1u;
-        const int nu = min(8, tr.u1 - (tr.u0 + t * 8));
+        const int nu = min(TU, tr.u1 - (tr.u0 + t * TU));
         const uint32_t idesc = idesc_bf16_f32(kBM, nu * 16);
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, args.err, abort_flag)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kBN);
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * TU * 16);
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(&full[stage], phase, args.err, abort_flag)) {
             ok = false;
@@ -188,11 +218,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tc_fence_after();
           const uint32_t sa = smem_u32(ring + (size_t)stage * sg.stride);
           const uint64_t da = sdesc_k_sw128(sa);
-          const uint64_t db = sdesc_k_sw128(sa + sg.a_bytes);
+          const uint64_t db = sdesc_k_sw128(sa + sg.b_off);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)  // 16 bf16 = 32 B per MMA along K: +2 in 16-B units
             umma_bf16(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
-          umma_commit(&empty[stage]);
+          if (CL == 1) umma_commit(&empty[stage]);
+          else umma_commit_mc(&empty[stage], cl_mask);  // the stage is free once every CTA read it
           if (++stage == sg.stages) {
             stage = 0;
             phase ^= 1u;
@@ -215,14 +246,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int t = 0; t < tr.num_tiles; ++t) {
       const int acc = t & 1;
       const uint32_t acc_phase = (uint32_t)(t >> 1) & 1u;
-      const int n0 = (tr.u0 + t * 8) * 16;
-      const int nt = min(8, tr.u1 - (tr.u0 + t * 8)) * 16;
+      const int n0 = (tr.u0 + t * TU) * 16;
+      const int nt = min(TU, tr.u1 - (tr.u0 + t * TU)) * 16;
       if (!mbar_wait(&tfull[acc], acc_phase, args.err, abort_flag)) break;
       tc_fence_after();
       if (warp_rows) {
         for (int c = 0; c < nt; c += 32) {
           float v[32];
-          tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kBN + c), v);
+          tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * TU * 16 + c), v);
           Epi::consume(st, ep, v, row, row_ok, n0 + c, min(32, nt - c), tr.col_end);
         }
       }
@@ -235,8 +266,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    tmem_dealloc(tmem_base, tmem_cols);
   }
+  if (CL > 1) cluster_sync();  // no CTA leaves while a peer may still write into it
 }
 
 // ---------------------------------------------------------------------------
