@@ -186,6 +186,24 @@ def traffic_record(M: int):
         return None
 
 
+# ---------------------------------------------------------------------------------- ranks
+
+def max_over_ranks(x: float, device) -> float:
+    """Largest value of x over all ranks (the slowest rank's time); x itself with one rank."""
+    import torch
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(units_per_rank: float, world: int, slowest_ms: float) -> float:
+    """Whole-job units per second when every rank processes units_per_rank in its own time
+    and the job ends with the slowest rank (replicas, no data exchange)."""
+    return world * units_per_rank / (slowest_ms * 1e-3)
+
+
 # ---------------------------------------------------------------------------------- ours
 
 def run_ours(args, rank, world, local_rank):
@@ -261,11 +279,7 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         torch.distributed.barrier()
     total_ms = sum(step_ms)
-    t_max = total_ms
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        t_max = float(t.item())
+    t_max = max_over_ranks(total_ms, dev)
     clk = clocks.stop()
 
     def graphed(fn):
@@ -310,11 +324,7 @@ def run_ours(args, rank, world, local_rank):
 
     e2e_ms = timed(e2e_step, args.steps, 3)
     assert np.array_equal(h_pid.numpy(), out["pid"].cpu().numpy())
-    e2e_total = sum(e2e_ms)
-    if world > 1:
-        t = torch.tensor([e2e_total], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_total = float(t.item())
+    e2e_total = max_over_ranks(sum(e2e_ms), dev)
 
     # other batch sizes of the metric (weights shared with the main workload)
     extra = {}
@@ -356,8 +366,8 @@ def run_ours(args, rank, world, local_rank):
     us = total_ms / args.steps * 1e3
     lm_us = statistics.mean(lm_ms) * 1e3
     achieved = lmhead_alg_bytes(sh, M) / (lm_us * 1e-6) / 1e9
-    value = world * B * args.steps / (t_max * 1e-3)
-    e2e_val = world * B * args.steps / (e2e_total * 1e-3)
+    value = replica_throughput(B * args.steps, world, t_max)
+    e2e_val = replica_throughput(B * args.steps, world, e2e_total)
     launches_per_step = sh.layers + 3
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,

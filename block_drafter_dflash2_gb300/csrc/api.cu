@@ -80,8 +80,8 @@ struct Plan {
   int a_tail_rows;  // rows of the last 128-row chunk, rounded up to 8
   int lm_parts;
   int conv_parts;
-  int chain_grid;  // > 0: all conv layers in one cooperative launch of this many CTAs
-  int chain_taps;  // the most projection rows one of its CTAs owns
+  bool chain;                // all conv layers in one cooperative launch
+  df::ConvChainPlan chain_plan;
   bool raw, greedy;
 };
 
@@ -131,18 +131,14 @@ dflash2_status_t make_plan(const dflash2_shape_t* s, Plan& p) {
       }
     }
     p.conv_parts = per < p_units ? per : p_units;
-    const int groups = p.H / 16;
-    const int grid = sms < groups ? sms : groups;
-    p.chain_taps = 2 * ((groups + grid - 1) / grid);
-    p.chain_grid = df::conv_chain_small_fits(p.M, p.H, p.chain_taps) ? grid : 0;
+    p.chain = df::conv_chain_plan(p.M, p.H, sms, &p.chain_plan);
   } else {
     p.n_rc = 1;
     p.lm_cluster = 1;
     p.a_tail_rows = 0;
     p.lm_parts = sms < v_units ? sms : v_units;
     p.conv_parts = 0;
-    p.chain_grid = 0;
-    p.chain_taps = 0;
+    p.chain = false;
   }
   if (p.lm_parts > 1024) p.lm_parts = 1024;
   return DFLASH2_OK;
@@ -174,7 +170,7 @@ Ws carve(const Plan& p, void* base) {
   };
   const size_t act = (size_t)p.M * p.H * p.esz;
   w.err = static_cast<int32_t*>(take(256));
-  w.bar = static_cast<unsigned*>(take(256));
+  w.bar = static_cast<unsigned*>(take(4096));  // one barrier counter per conv row block
   w.conv0 = take(act);
   w.conv1 = take(act);
   w.part_val = static_cast<float*>(take((size_t)p.lm_parts * p.M * 16 * 4));
@@ -202,9 +198,9 @@ dflash2_status_t run_conv(const Plan& p, const void* x, const void* conv_w, void
                           cudaStream_t s) {
   const size_t act = (size_t)p.M * p.H * p.esz;
   if (p.NL == 0) return cuda_status(cudaMemcpyAsync(y, x, act, cudaMemcpyDeviceToDevice, s));
-  if (p.bf16 && p.chain_grid > 0)
-    return cuda_status(df::launch_conv_chain_small(x, conv_w, w.conv0, w.conv1, y, p.M, p.H, p.T, p.NL,
-                                                   p.raw ? 1 : 0, p.chain_taps, w.bar, w.err, p.chain_grid, s));
+  if (p.bf16 && p.chain)
+    return cuda_status(df::launch_conv_chain(p.chain_plan, x, conv_w, w.conv0, w.conv1, y, p.M, p.H, p.T, p.NL,
+                                             p.raw ? 1 : 0, w.bar, w.err, s));
   const void* cur = x;
   for (int l = 0; l < p.NL; ++l) {
     void* out = (l == p.NL - 1) ? y : ((l % 2 == 0) ? w.conv0 : w.conv1);

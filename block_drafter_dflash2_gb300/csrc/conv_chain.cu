@@ -1,25 +1,27 @@
-// All conv layers in one cooperative launch, for a small number of rows (M <= 64, bf16).
+// All conv layers in one cooperative launch (bf16), on the tensor cores through mma.sync.
 //
-// Each CTA owns a contiguous range of channel groups [g0, g1) for every layer (2-4 groups at
-// the page shape: 320 groups over the SMs), i.e. projection rows 2*g0 .. 2*g1 of each layer's
-// weight, which are contiguous in memory. Per layer:
-//   1. taps: P[m][q] = x[m] . W[2*g0 + q] for every row m and the CTA's taps q, on the tensor
-//      cores (mma.sync m16n8k16, bf16 in, fp32 accumulate); each warp takes 1/8 of the
-//      hidden dimension and the 8 warps' partial tiles are summed in shared memory;
+// CTA (rb, gb) owns a block of rows [rb*RB, rb*RB + RB) and a contiguous range of channel
+// groups [g0, g1) for every layer, i.e. projection rows 2*g0 .. 2*g1 of each layer's weight
+// (contiguous in memory). RB is 16 or 64 rows (one or four 16-row tiles); row blocks are
+// independent of each other, so each has its own grid barrier. Per layer:
+//   1. taps: P[m][q] = x[m] . W[2*g0 + q] for the block's rows m and the CTA's taps q with
+//      mma.sync m16n8k16 (bf16 in, fp32 accumulate). Warp w takes row tile w % MT and the
+//      hidden slice w / MT of 8 / MT; the slices' partial tiles are summed in shared memory.
+//      The 16 k-slots of one MMA may hold any 16 of a 32-wide chunk's positions as long as A
+//      and B agree, so lane (g = lane/4, j = lane%4) feeds rows g, g+8 (A) and tap row g (B)
+//      with one 16-byte load each for positions 8j..8j+7: 8j..8j+3 go to the first MMA and
+//      8j+4..8j+7 to the second.
 //   2. mix: (a, b) = softmax(P[m][2j], P[m][2j+1]) (raw taps on request), and
 //      y[m][c] = a * x[m-1][c] + b * x[m][c] for the group's 16 channels, x[-1] = 0 at each
 //      block start, rounded to bf16 and written to the layer's output buffer;
-//   3. a grid barrier (every CTA needs every channel of the next layer's input).
-// Weight slices arrive in shared memory by bulk async copies, requested as soon as the buffer
-// they go to is free, so their latency hides behind the mix and the barrier.
-// Two variants:
-//   kStageX (M <= 16): the layer's whole input block x [M, H] (contiguous) is copied into
-//     shared memory by one bulk copy after the barrier; taps and mix read it there. The weight
-//     slice is single-buffered to make room.
-//   otherwise: x is read from L2 with .cg loads (which skip the non-coherent L1, since the
-//     buffers are rewritten between layers) and the weight slice is double-buffered.
-// The barrier is an atomic counter in the workspace (zeroed by the host before the launch)
-// with a bounded spin: on timeout the kernel sets DFLASH2_DEVERR_WAIT_TIMEOUT and stops.
+//   3. the row block's barrier (its CTAs need every channel of the next layer's input rows).
+// Variants (template flags): the block's input rows x are staged in shared memory by one bulk
+// copy after the barrier (kStageX, 16-row blocks), or read from L2 with .cg loads (which skip
+// the non-coherent L1: the buffers are rewritten between layers); the weight slice is staged
+// in shared memory by a bulk copy requested as soon as the previous layer's taps are done
+// (kStageW), or read from global memory after an L2 prefetch issued a layer ahead.
+// Barriers are atomic counters in the workspace (zeroed by the host before the launch) with
+// a bounded spin: on timeout the kernel sets DFLASH2_DEVERR_WAIT_TIMEOUT and stops.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -32,9 +34,6 @@ namespace df {
 namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kTaps = 8;       // taps per CTA at most (4 groups)
-constexpr int kMaxRows = 64;
-constexpr int kStageRows = 16;  // the staged variant's row limit
 
 DF_DEV void bulk_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -43,19 +42,23 @@ DF_DEV void bulk_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes, uint6
                : "memory");
 }
 
+DF_DEV void prefetch_l2(const void* gmem_src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gmem_src), "r"(bytes) : "memory");
+}
+
 DF_DEV uint32_t ld_acquire(const unsigned* p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 
-// Grid barrier number `round` (1, 2, ...): every CTA adds one, then waits for round * grid.
-DF_DEV bool grid_barrier(unsigned* count, unsigned round, int32_t* err, volatile int* stop) {
+// Barrier number `round` (1, 2, ...) of `members` CTAs sharing `count`.
+DF_DEV bool group_barrier(unsigned* count, unsigned round, unsigned members, int32_t* err, volatile int* stop) {
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
     atomicAdd(count, 1u);
-    const unsigned target = round * gridDim.x;
+    const unsigned target = round * members;
     const uint64_t t0 = globaltimer_ns();
     while (ld_acquire(count) < target) {
       __nanosleep(32);
@@ -81,150 +84,147 @@ DF_DEV void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-template <bool kStageX>
-DF_DEV uint4 load_x16(const __nv_bfloat16* p) {
-  if constexpr (kStageX) return *reinterpret_cast<const uint4*>(p);
+template <bool kSmem>
+DF_DEV uint4 ld16(const __nv_bfloat16* p) {
+  if constexpr (kSmem) return *reinterpret_cast<const uint4*>(p);
   else return __ldcg(reinterpret_cast<const uint4*>(p));
 }
 
-template <bool kStageX>
+template <bool kStageX, bool kStageW, int kMT, int kNT>
 __global__ void __launch_bounds__(kThreads, 1)
-    conv_chain_small_kernel(const __nv_bfloat16* __restrict__ x0, const __nv_bfloat16* __restrict__ W,
-                            __nv_bfloat16* buf0, __nv_bfloat16* buf1, __nv_bfloat16* z_out, int M, int H, int T,
-                            int NL, int raw, int wtaps, unsigned* bar_count, int32_t* err) {
-  constexpr int kRows = kStageX ? kStageRows : kMaxRows;
-  constexpr int kMT = kRows / 16;  // row tiles of 16
+    conv_chain_kernel(const __nv_bfloat16* __restrict__ x0, const __nv_bfloat16* __restrict__ W,
+                      __nv_bfloat16* buf0, __nv_bfloat16* buf1, __nv_bfloat16* z_out, int M, int H, int T, int NL,
+                      int raw, int GBn, int wtaps, unsigned* bar_counts, int32_t* err) {
+  constexpr int RB = 16 * kMT;          // rows per block
+  constexpr int kSlices = kWarps / kMT;  // hidden slices per row tile
+  constexpr int TQ = kNT * 8;            // taps per CTA, padded
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  __shared__ uint64_t wbar[2], xbar;
-  __shared__ float red[kWarps][kRows * kTaps];
-  __shared__ float taps_s[kRows][kTaps];
+  __shared__ uint64_t wbar, xbar;
   __shared__ int stop;
-  constexpr int kBufs = kStageX ? 1 : 2;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rb = blockIdx.x / GBn, gb = blockIdx.x % GBn;
+  const int r0 = rb * RB, nrows = min(RB, M - r0);
   const int G = H / 16, P = 2 * G;
-  const int g0 = (int)((int64_t)blockIdx.x * G / gridDim.x);
-  const int g1 = (int)((int64_t)(blockIdx.x + 1) * G / gridDim.x);
+  const int g0 = (int)((int64_t)gb * G / GBn);
+  const int g1 = (int)((int64_t)(gb + 1) * G / GBn);
   const int ntaps = 2 * (g1 - g0);
   const uint32_t slice_bytes = (uint32_t)ntaps * H * 2;
-  // weight buffers hold `wtaps` rows (the most any CTA owns); the staged x block follows them
-  __nv_bfloat16* wbuf[2] = {reinterpret_cast<__nv_bfloat16*>(smem_raw),
-                            reinterpret_cast<__nv_bfloat16*>(smem_raw) + (size_t)wtaps * H};
-  __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(smem_raw) + (size_t)kBufs * wtaps * H;  // kStageX only
-  const uint32_t x_bytes = (uint32_t)M * H * 2;
+  // shared memory: [weight slice (kStageW)] [x rows (kStageX)] [partial tiles] [taps]
+  uint8_t* p = smem_raw;
+  __nv_bfloat16* ws = reinterpret_cast<__nv_bfloat16*>(p);
+  if constexpr (kStageW) p += (size_t)wtaps * H * 2;
+  __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(p);
+  if constexpr (kStageX) p += (size_t)RB * H * 2;
+  float* red = reinterpret_cast<float*>(p);  // [kSlices][RB][TQ]
+  p += (size_t)kSlices * RB * TQ * 4;
+  float* taps_s = reinterpret_cast<float*>(p);  // [RB][TQ]
+  unsigned* my_bar = bar_counts + rb;
 
-  int last_issued[2] = {-1, -1};  // thread 0: newest layer requested into each buffer
   if (tid == 0) {
     stop = 0;
-    mbar_init(&wbar[0], 1);
-    mbar_init(&wbar[1], 1);
+    mbar_init(&wbar, 1);
     mbar_init(&xbar, 1);
     fence_barrier_init();
-    for (int l = 0; l < kBufs && l < NL; ++l) {
-      mbar_arrive_expect_tx(&wbar[l], slice_bytes);
-      bulk_g2s(wbuf[l], W + ((size_t)l * P + 2 * g0) * H, slice_bytes, &wbar[l]);
-      last_issued[l] = l;
+    if constexpr (kStageW) {
+      mbar_arrive_expect_tx(&wbar, slice_bytes);
+      bulk_g2s(ws, W + (size_t)(2 * g0) * H, slice_bytes, &wbar);
+    } else {
+      prefetch_l2(W + (size_t)(2 * g0) * H, slice_bytes);
     }
   }
   __syncthreads();
 
-  uint32_t xphase = 0;
+  const int mt = warp % kMT, ks = warp / kMT;
+  const int kw = H / kSlices;
+  const int kbeg = ks * kw;
+  const int g = lane >> 2, j = lane & 3;
+  // rows past the block's end read its last row (their products land in dropped accumulator rows)
+  const int rlo = min(mt * 16 + g, nrows - 1), rhi = min(mt * 16 + g + 8, nrows - 1);
+
+  uint32_t wphase = 0, xphase = 0;
+  bool w_pending = kStageW;  // thread 0 issued a weight copy not yet waited for
   for (int l = 0; l < NL; ++l) {
     const __nv_bfloat16* xin_g = (l == 0) ? x0 : ((l - 1) % 2 == 0 ? buf0 : buf1);
     __nv_bfloat16* xout = (l == NL - 1) ? z_out : (l % 2 == 0 ? buf0 : buf1);
-    const int wb = l % kBufs;
-    const __nv_bfloat16* ws = wbuf[wb];
-    const __nv_bfloat16* xin = xin_g;
+    const __nv_bfloat16* wl = W + ((size_t)l * P + 2 * g0) * H;  // this layer's slice
+    if (!kStageW && tid == 0 && l + 1 < NL) prefetch_l2(wl + (size_t)P * H, slice_bytes);
+    const __nv_bfloat16* xb = xin_g + (size_t)r0 * H;  // the block's first row
     if constexpr (kStageX) {
       if (tid == 0) {
-        // the block was written by other CTAs' generic stores before the barrier; order them
-        // before this async-proxy read
+        // rows written by other CTAs' generic stores before the barrier; order them before
+        // this async-proxy read
         asm volatile("fence.proxy.async.global;" ::: "memory");
-        mbar_arrive_expect_tx(&xbar, x_bytes);
-        bulk_g2s(xs, xin_g, x_bytes, &xbar);
+        mbar_arrive_expect_tx(&xbar, (uint32_t)nrows * H * 2);
+        bulk_g2s(xs, xb, (uint32_t)nrows * H * 2, &xbar);
       }
-      xin = xs;
       if (!mbar_wait(&xbar, xphase, err, &stop)) break;
       xphase ^= 1u;
     }
-    if (!mbar_wait(&wbar[wb], (uint32_t)(l / kBufs) & 1u, err, &stop)) break;
+    if constexpr (kStageW) {
+      if (!mbar_wait(&wbar, wphase, err, &stop)) break;
+      wphase ^= 1u;
+      if (tid == 0) w_pending = false;
+    }
+    const __nv_bfloat16* xa_base = kStageX ? xs : xb;
+    const __nv_bfloat16* wb_base = kStageW ? ws : wl;
 
-    // ---- 1. taps for every row on the tensor cores. Warp w takes the hidden range
-    // [w*H/8, (w+1)*H/8) in chunks of 32. The 16 k-slots of one MMA may hold any 16 of the
-    // chunk's positions as long as A and B agree, so lane (g = lane/4, j = lane%4) loads 8
-    // consecutive positions 8j..8j+7 of rows g and g+8 (A) and of tap row g (B) as single
-    // 16-byte loads: positions 8j..8j+3 feed the first MMA and 8j+4..8j+7 the second.
+    // ---- 1. taps
     {
-      const int g = lane >> 2, j = lane & 3;
-      const int kw = H / kWarps;
-      const int kbeg = warp * kw;
-      const int mtiles = (M + 15) / 16;  // at most kRows / 16
-      float acc[kMT][4];
+      float acc[kNT][4];
 #pragma unroll
-      for (int mt = 0; mt < kMT; ++mt)
+      for (int nt = 0; nt < kNT; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
-      // rows past M read row M-1 (their products land in accumulator rows that are dropped)
-      int rlo[kMT], rhi[kMT];
+        for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+      bool tap_ok[kNT];
 #pragma unroll
-      for (int mt = 0; mt < kMT; ++mt) {
-        rlo[mt] = min(mt * 16 + g, M - 1);
-        rhi[mt] = min(mt * 16 + g + 8, M - 1);
-      }
-      const bool tap_ok = g < ntaps;
-      // unrolled so that several chunks' loads are in flight before their MMAs consume them
-#pragma unroll 4
+      for (int nt = 0; nt < kNT; ++nt) tap_ok[nt] = nt * 8 + g < ntaps;
+#pragma unroll 2
       for (int k0 = kbeg; k0 < kbeg + kw; k0 += 32) {
         const int kk = k0 + 8 * j;
-        uint4 xa[kMT], xb[kMT];
+        const uint4 xa = ld16<kStageX>(xa_base + (size_t)rlo * H + kk);
+        const uint4 xc = ld16<kStageX>(xa_base + (size_t)rhi * H + kk);
+        uint4 wv[kNT];
 #pragma unroll
-        for (int mt = 0; mt < kMT; ++mt) {
-          if (mt < mtiles) {
-            xa[mt] = load_x16<kStageX>(xin + (size_t)rlo[mt] * H + kk);
-            xb[mt] = load_x16<kStageX>(xin + (size_t)rhi[mt] * H + kk);
-          }
-        }
-        const uint4 wv = tap_ok ? *reinterpret_cast<const uint4*>(ws + (size_t)g * H + kk) : make_uint4(0, 0, 0, 0);
+        for (int nt = 0; nt < kNT; ++nt)
+          wv[nt] = tap_ok[nt] ? ld16<kStageW>(wb_base + (size_t)(nt * 8 + g) * H + kk) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-        for (int mt = 0; mt < kMT; ++mt) {
-          if (mt < mtiles) {
-            mma_16816(acc[mt], xa[mt].x, xb[mt].x, xa[mt].y, xb[mt].y, wv.x, wv.y);
-            mma_16816(acc[mt], xa[mt].z, xb[mt].z, xa[mt].w, xb[mt].w, wv.z, wv.w);
-          }
+        for (int nt = 0; nt < kNT; ++nt) {
+          mma_16816(acc[nt], xa.x, xc.x, xa.y, xc.y, wv[nt].x, wv[nt].y);
+          mma_16816(acc[nt], xa.z, xc.z, xa.w, xc.w, wv[nt].z, wv[nt].w);
         }
       }
-      // accumulator layout: acc[mt][0..1] = row mt*16+g, taps 2j, 2j+1; [2..3] = row +8
+      // accumulator layout: acc[nt][0..1] = row mt*16+g, taps nt*8+2j, +1; [2..3] = row +8
+      float* rw = red + (size_t)ks * RB * TQ;
 #pragma unroll
-      for (int mt = 0; mt < kMT; ++mt) {
-        if (mt < mtiles) {
-          red[warp][(mt * 16 + g) * kTaps + 2 * j] = acc[mt][0];
-          red[warp][(mt * 16 + g) * kTaps + 2 * j + 1] = acc[mt][1];
-          red[warp][(mt * 16 + g + 8) * kTaps + 2 * j] = acc[mt][2];
-          red[warp][(mt * 16 + g + 8) * kTaps + 2 * j + 1] = acc[mt][3];
-        }
+      for (int nt = 0; nt < kNT; ++nt) {
+        rw[(mt * 16 + g) * TQ + nt * 8 + 2 * j] = acc[nt][0];
+        rw[(mt * 16 + g) * TQ + nt * 8 + 2 * j + 1] = acc[nt][1];
+        rw[(mt * 16 + g + 8) * TQ + nt * 8 + 2 * j] = acc[nt][2];
+        rw[(mt * 16 + g + 8) * TQ + nt * 8 + 2 * j + 1] = acc[nt][3];
       }
       __syncthreads();
-      for (int e = tid; e < M * kTaps; e += kThreads) {
+      for (int e = tid; e < nrows * TQ; e += kThreads) {
         float t = 0.f;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) t += red[w][e];
-        taps_s[e / kTaps][e % kTaps] = t;
+        for (int s = 0; s < kSlices; ++s) t += red[(size_t)s * RB * TQ + e];
+        taps_s[e] = t;
       }
       __syncthreads();
     }
-    // the weight buffer of layer l is free: request layer l + kBufs's slice into it
-    if (tid == 0 && l + kBufs < NL) {
+    // the staged weight slice is free: request the next layer's
+    if (kStageW && tid == 0 && l + 1 < NL) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive_expect_tx(&wbar[wb], slice_bytes);
-      bulk_g2s(wbuf[wb], W + ((size_t)(l + kBufs) * P + 2 * g0) * H, slice_bytes, &wbar[wb]);
-      last_issued[wb] = l + kBufs;
+      mbar_arrive_expect_tx(&wbar, slice_bytes);
+      bulk_g2s(ws, wl + (size_t)P * H, slice_bytes, &wbar);
+      w_pending = true;
     }
 
-    // ---- 2. mix: 16-byte pieces (8 channels) of the CTA's channels, every row
+    // ---- 2. mix: 16-byte pieces (8 channels) of the CTA's channels, every row of the block
     const int pieces = (g1 - g0) * 2;  // two 8-channel pieces per group
-    for (int e = tid; e < M * pieces; e += kThreads) {
+    for (int e = tid; e < nrows * pieces; e += kThreads) {
       const int m = e / pieces, pc = e % pieces;
       const int jg = pc >> 1;  // group index within the CTA
-      const float p0 = taps_s[m][2 * jg], p1 = taps_s[m][2 * jg + 1];
+      const float p0 = taps_s[m * TQ + 2 * jg], p1 = taps_s[m * TQ + 2 * jg + 1];
       float a, b;
       if (raw) {
         a = p0;
@@ -237,8 +237,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         b = e1 * inv;
       }
       const int c0 = (g0 + jg) * 16 + (pc & 1) * 8;
-      const uint4 cur = load_x16<kStageX>(xin + (size_t)m * H + c0);
-      const uint4 prv = (m % T) != 0 ? load_x16<kStageX>(xin + (size_t)(m - 1) * H + c0) : make_uint4(0, 0, 0, 0);
+      const uint4 cur = ld16<kStageX>(xa_base + (size_t)m * H + c0);
+      uint4 prv = make_uint4(0, 0, 0, 0);
+      if ((r0 + m) % T != 0)  // the previous row of the same sequence (outside the block if m == 0)
+        prv = m > 0 ? ld16<kStageX>(xa_base + (size_t)(m - 1) * H + c0)
+                    : __ldcg(reinterpret_cast<const uint4*>(xb - H + c0));
       const __nv_bfloat162* c2 = reinterpret_cast<const __nv_bfloat162*>(&cur);
       const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&prv);
       uint4 out;
@@ -249,53 +252,74 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float2 pf = __bfloat1622float2(p2[k]);
         o2[k] = __floats2bfloat162_rn(fmaf(a, pf.x, b * cf.x), fmaf(a, pf.y, b * cf.y));
       }
-      *reinterpret_cast<uint4*>(xout + (size_t)m * H + c0) = out;
+      *reinterpret_cast<uint4*>(xout + (size_t)(r0 + m) * H + c0) = out;
     }
-    if (l + 1 < NL && !grid_barrier(bar_count, (unsigned)(l + 1), err, &stop)) break;
+    if (l + 1 < NL && !group_barrier(my_bar, (unsigned)(l + 1), (unsigned)GBn, err, &stop)) break;
   }
   // no copy may still be landing in shared memory when the CTA exits
-  if (tid == 0) {
-    for (int b = 0; b < kBufs; ++b)
-      if (last_issued[b] >= 0) mbar_wait(&wbar[b], (uint32_t)(last_issued[b] / kBufs) & 1u, err, nullptr);
-  }
+  if (kStageW && tid == 0 && w_pending) mbar_wait(&wbar, wphase, err, nullptr);
   __syncthreads();
 }
+
+// Variants: (stage x, stage weights, row tiles, tap tiles).
+struct Variant {
+  bool sx, sw;
+  int mt, nt;
+};
+constexpr Variant kVariants[] = {{true, true, 1, 1}, {true, false, 1, 3}, {false, true, 4, 3}, {false, false, 4, 9}};
+
+size_t variant_smem(const Variant& v, int H, int wtaps) {
+  const int RB = 16 * v.mt, slices = kWarps / v.mt, TQ = v.nt * 8;
+  return (v.sw ? (size_t)wtaps * H * 2 : 0) + (v.sx ? (size_t)RB * H * 2 : 0) + (size_t)slices * RB * TQ * 4 +
+         (size_t)RB * TQ * 4;
+}
+
+constexpr size_t kSmemLimit = 227 * 1024 - 256;  // minus the static barriers
 }  // namespace
 
-// Dynamic shared memory of one variant: the weight buffer(s) of `wtaps` rows, and for the
-// staged variant the x block.
-static size_t chain_smem(bool stage, int M, int H, int wtaps) {
-  return (size_t)(stage ? 1 : 2) * wtaps * H * 2 + (stage ? (size_t)M * H * 2 : 0);
+bool conv_chain_plan(int M, int H, int sms, ConvChainPlan* out) {
+  if (H % 256 != 0 || M < 1 || sms < 1) return false;
+  const int G = H / 16;
+  // the first variant whose row tiles, tap capacity and shared memory fit
+  for (int vi = 0; vi < 4; ++vi) {
+    const Variant& v = kVariants[vi];
+    const int RB = 16 * v.mt;
+    if (vi == 0 && M > 16) continue;    // one 16-row block with all CTAs on the groups
+    if (v.mt == 1 && M > 64) continue;  // 16-row blocks only for small M
+    if (v.mt == 4 && M <= 64) continue;
+    const int RBn = (M + RB - 1) / RB;
+    if (RBn > sms) continue;
+    int GBn = sms / RBn;
+    if (GBn > G) GBn = G;
+    const int taps = 2 * ((G + GBn - 1) / GBn);
+    if (taps > v.nt * 8) continue;
+    if (variant_smem(v, H, taps) > kSmemLimit) continue;
+    out->variant = vi;
+    out->row_blocks = RBn;
+    out->group_blocks = GBn;
+    out->wtaps = taps;
+    out->smem = variant_smem(v, H, taps);
+    return true;
+  }
+  return false;
 }
 
-// Largest dynamic shared memory a variant may ask for: 227 KB minus its static arrays
-// (reduction tiles and taps) and a margin for the barriers.
-static size_t chain_smem_limit(bool stage) {
-  const size_t rows = stage ? kStageRows : kMaxRows;
-  return 227 * 1024 - (size_t)kWarps * rows * kTaps * 4 - rows * kTaps * 4 - 256;
-}
-
-bool conv_chain_small_fits(int M, int H, int wtaps) {
-  if (M > kMaxRows || wtaps > kTaps || H % 256 != 0) return false;
-  return chain_smem(false, M, H, wtaps) <= chain_smem_limit(false);
-}
-
-cudaError_t launch_conv_chain_small(const void* x, const void* conv_w, void* buf0, void* buf1, void* z, int M,
-                                    int H, int T, int NL, int raw, int wtaps, unsigned* bar_count, int32_t* err,
-                                    int grid, cudaStream_t s) {
-  if (!conv_chain_small_fits(M, H, wtaps)) return cudaErrorInvalidValue;
-  const bool stage = M <= kStageRows && chain_smem(true, M, H, wtaps) <= chain_smem_limit(true);
-  const size_t smem = chain_smem(stage, M, H, wtaps);
-  const void* fn = stage ? reinterpret_cast<const void*>(conv_chain_small_kernel<true>)
-                         : reinterpret_cast<const void*>(conv_chain_small_kernel<false>);
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+cudaError_t launch_conv_chain(const ConvChainPlan& pl, const void* x, const void* conv_w, void* buf0, void* buf1,
+                              void* z, int M, int H, int T, int NL, int raw, unsigned* bar_counts, int32_t* err,
+                              cudaStream_t s) {
+  const void* fns[4] = {reinterpret_cast<const void*>(conv_chain_kernel<true, true, 1, 1>),
+                        reinterpret_cast<const void*>(conv_chain_kernel<true, false, 1, 3>),
+                        reinterpret_cast<const void*>(conv_chain_kernel<false, true, 4, 3>),
+                        reinterpret_cast<const void*>(conv_chain_kernel<false, false, 4, 9>)};
+  if (pl.variant < 0 || pl.variant > 3) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(fns[pl.variant], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
   if (e != cudaSuccess) return e;
-  e = cudaMemsetAsync(bar_count, 0, sizeof(unsigned), s);
+  e = cudaMemsetAsync(bar_counts, 0, sizeof(unsigned) * pl.row_blocks, s);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
+  cfg.gridDim = dim3(pl.row_blocks * pl.group_blocks);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = pl.smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
@@ -307,10 +331,24 @@ cudaError_t launch_conv_chain_small(const void* x, const void* conv_w, void* buf
   __nv_bfloat16* b0 = reinterpret_cast<__nv_bfloat16*>(buf0);
   __nv_bfloat16* b1 = reinterpret_cast<__nv_bfloat16*>(buf1);
   __nv_bfloat16* zb = reinterpret_cast<__nv_bfloat16*>(z);
-  e = stage ? cudaLaunchKernelEx(&cfg, conv_chain_small_kernel<true>, xb, wb, b0, b1, zb, M, H, T, NL, raw, wtaps,
-                                 bar_count, err)
-            : cudaLaunchKernelEx(&cfg, conv_chain_small_kernel<false>, xb, wb, b0, b1, zb, M, H, T, NL, raw, wtaps,
-                                 bar_count, err);
+  switch (pl.variant) {
+    case 0:
+      e = cudaLaunchKernelEx(&cfg, conv_chain_kernel<true, true, 1, 1>, xb, wb, b0, b1, zb, M, H, T, NL, raw,
+                             pl.group_blocks, pl.wtaps, bar_counts, err);
+      break;
+    case 1:
+      e = cudaLaunchKernelEx(&cfg, conv_chain_kernel<true, false, 1, 3>, xb, wb, b0, b1, zb, M, H, T, NL, raw,
+                             pl.group_blocks, pl.wtaps, bar_counts, err);
+      break;
+    case 2:
+      e = cudaLaunchKernelEx(&cfg, conv_chain_kernel<false, true, 4, 3>, xb, wb, b0, b1, zb, M, H, T, NL, raw,
+                             pl.group_blocks, pl.wtaps, bar_counts, err);
+      break;
+    default:
+      e = cudaLaunchKernelEx(&cfg, conv_chain_kernel<false, false, 4, 9>, xb, wb, b0, b1, zb, M, H, T, NL, raw,
+                             pl.group_blocks, pl.wtaps, bar_counts, err);
+      break;
+  }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

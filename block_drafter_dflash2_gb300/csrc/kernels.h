@@ -25,13 +25,20 @@ cudaError_t launch_conv_layer_bf16(const CUtensorMap& a, const CUtensorMap& a_ta
                                    const TcGemmArgs& args, const void* x, void* y, int T, int raw,
                                    cudaStream_t s);
 
-// All conv layers in one cooperative launch for M <= 64 rows (bf16); `grid` CTAs, each owning
-// a contiguous range of at most 4 channel groups. Zeroes *bar_count on the stream first.
-// `wtaps` = the most projection rows any CTA owns (2 * ceil(groups / grid)).
-bool conv_chain_small_fits(int M, int H, int wtaps);
-cudaError_t launch_conv_chain_small(const void* x, const void* conv_w, void* buf0, void* buf1, void* z, int M,
-                                    int H, int T, int NL, int raw, int wtaps, unsigned* bar_count, int32_t* err,
-                                    int grid, cudaStream_t s);
+// All conv layers in one cooperative launch (bf16, hidden % 256 == 0): row blocks x group
+// blocks of CTAs, mma.sync taps; conv_chain_plan picks the kernel variant and the grid for the
+// device's SM count (false if no variant fits). Zeroes the row blocks' barrier counters first.
+struct ConvChainPlan {
+  int variant;       // kernel instantiation
+  int row_blocks;    // blocks of 16 or 64 rows
+  int group_blocks;  // CTAs per row block, each owning a range of channel groups
+  int wtaps;         // the most projection rows one CTA owns
+  size_t smem;       // dynamic shared memory per CTA
+};
+bool conv_chain_plan(int M, int H, int sms, ConvChainPlan* out);
+cudaError_t launch_conv_chain(const ConvChainPlan& pl, const void* x, const void* conv_w, void* buf0, void* buf1,
+                              void* z, int M, int H, int T, int NL, int raw, unsigned* bar_counts, int32_t* err,
+                              cudaStream_t s);
 
 // fp32 instantiations (small sizes).
 cudaError_t launch_conv_layer_f32(const float* x, const float* w, float* y, int M, int H, int T, int raw,

@@ -343,13 +343,21 @@ def draft_tail(inp: dict, shape, seqs=None, row_block: int = 64) -> dict:
     (K+1)-th logits and max logit per row, tau, path_idx/path_ids/score, the list-Viterbi
     best/second scores.
     """
-    B, T, H, K = shape.batch, shape.block, shape.hidden, shape.top_k
+    B = shape.batch
     seqs = list(range(B)) if seqs is None else list(seqs)
     hidden = np.asarray(inp["hidden"])[seqs]
-    anchor = np.asarray(inp["anchor"])[seqs]
     z = conv_chain(hidden, inp["conv_w"], shape.dtype, shape.group_size, shape.taps)
+    return select_from_z(z, inp, shape, seqs, row_block)
+
+
+def select_from_z(z: np.ndarray, inp: dict, shape, seqs, row_block: int = 64) -> dict:
+    """The tail after the conv, on given conv outputs z [b, T, H] of the listed sequences:
+    logits, lse, top-K, transitions from those sequences' anchors, Viterbi and margins."""
+    T, H, K = shape.block, shape.hidden, shape.top_k
+    seqs = list(seqs)
+    anchor = np.asarray(inp["anchor"])[seqs]
     nb = len(seqs)
-    rows = z.reshape(nb * T, H)
+    rows = np.asarray(z).reshape(nb * T, H)
     M = rows.shape[0]
     ids = np.empty((M, K), dtype=np.int32)
     vals = np.empty((M, K), dtype=np.float32)
@@ -368,9 +376,8 @@ def draft_tail(inp: dict, shape, seqs=None, row_block: int = 64) -> dict:
     path_idx, score = viterbi(lp, tau)
     path_ids = np.take_along_axis(cids, path_idx[..., None].astype(np.int64), axis=2)[..., 0]
     best, second = viterbi_two_best(lp, tau)
-    return dict(z=z, cand_ids=cids, cand_lp=lp, cand_logit=vals.reshape(nb, T, K),
+    return dict(z=np.asarray(z), cand_ids=cids, cand_lp=lp, cand_logit=vals.reshape(nb, T, K),
                 next_logit=nxt.reshape(nb, T), max_logit=lmax.reshape(nb, T),
                 lse=lse.reshape(nb, T), lse32=lse.astype(np.float32).reshape(nb, T),
                 tau=tau, path_idx=path_idx, path_ids=path_ids.astype(np.int32), score=score,
                 best=best, second=second, seqs=np.asarray(seqs))
-
