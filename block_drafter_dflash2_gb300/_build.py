@@ -12,7 +12,7 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libdflash2.so")
 BUILD = os.path.join(HERE, "_build")
-SOURCES = ["api.cu", "lmhead_tc.cu", "conv_chain.cu", "merge.cu", "viterbi.cu", "simt_f32.cu"]
+SOURCES = ["api.cu", "lmhead_tc.cu", "conv_chain.cu", "conv_splitk.cu", "merge.cu", "viterbi.cu", "simt_f32.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

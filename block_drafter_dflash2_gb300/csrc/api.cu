@@ -71,6 +71,10 @@ bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Row counts up to this use the chain kernel that reads whole rows per CTA; above it the
+// split-K chain, whose per-CTA traffic does not grow with the row count as fast.
+constexpr int kChainMaxRows = 16;
+
 struct Plan {
   int B, T, H, V, K, R, NL, P, M;
   bool bf16;
@@ -80,8 +84,10 @@ struct Plan {
   int a_tail_rows;  // rows of the last 128-row chunk, rounded up to 8
   int lm_parts;
   int conv_parts;
-  bool chain;                // all conv layers in one cooperative launch
+  bool chain;                // all conv layers in one cooperative launch (small M)
   df::ConvChainPlan chain_plan;
+  bool split;                // all conv layers in one cooperative launch, split-K (larger M)
+  df::ConvSplitPlan split_plan;
   bool raw, greedy;
 };
 
@@ -131,7 +137,8 @@ dflash2_status_t make_plan(const dflash2_shape_t* s, Plan& p) {
       }
     }
     p.conv_parts = per < p_units ? per : p_units;
-    p.chain = df::conv_chain_plan(p.M, p.H, sms, &p.chain_plan);
+    p.split = p.M > kChainMaxRows && p.NL > 0 && df::conv_splitk_plan(p.M, p.H, p.NL, sms, &p.split_plan);
+    p.chain = !p.split && df::conv_chain_plan(p.M, p.H, sms, &p.chain_plan);
   } else {
     p.n_rc = 1;
     p.lm_cluster = 1;
@@ -139,6 +146,7 @@ dflash2_status_t make_plan(const dflash2_shape_t* s, Plan& p) {
     p.lm_parts = sms < v_units ? sms : v_units;
     p.conv_parts = 0;
     p.chain = false;
+    p.split = false;
   }
   if (p.lm_parts > 1024) p.lm_parts = 1024;
   return DFLASH2_OK;
@@ -151,6 +159,7 @@ struct Ws {
   unsigned* bar;
   void* conv0;
   void* conv1;
+  float* conv_part;
   float* part_val;
   int32_t* part_id;
   float* part_ms;
@@ -173,6 +182,7 @@ Ws carve(const Plan& p, void* base) {
   w.bar = static_cast<unsigned*>(take(4096));  // one barrier counter per conv row block
   w.conv0 = take(act);
   w.conv1 = take(act);
+  w.conv_part = static_cast<float*>(take(p.split ? p.split_plan.part_bytes : 0));
   w.part_val = static_cast<float*>(take((size_t)p.lm_parts * p.M * 16 * 4));
   w.part_id = static_cast<int32_t*>(take((size_t)p.lm_parts * p.M * 16 * 4));
   w.part_ms = static_cast<float*>(take((size_t)p.lm_parts * p.M * 2 * 4));
@@ -198,6 +208,18 @@ dflash2_status_t run_conv(const Plan& p, const void* x, const void* conv_w, void
                           cudaStream_t s) {
   const size_t act = (size_t)p.M * p.H * p.esz;
   if (p.NL == 0) return cuda_status(cudaMemcpyAsync(y, x, act, cudaMemcpyDeviceToDevice, s));
+  if (p.bf16 && p.split) {
+    const df::ConvSplitPlan& sp = p.split_plan;
+    CUtensorMap maps[7];
+    const void* srcs[3] = {x, w.conv0, w.conv1};
+    for (int i = 0; i < 3; ++i)
+      if (!encode_bf16_2d(&maps[2 * i], srcs[i], p.H, p.M, 128) ||
+          !encode_bf16_2d(&maps[2 * i + 1], srcs[i], p.H, p.M, sp.a_tail_rows))
+        return DFLASH2_ERR_CUDA;
+    if (!encode_bf16_2d(&maps[6], conv_w, p.H, (uint64_t)p.NL * p.P, sp.Nt)) return DFLASH2_ERR_CUDA;
+    return cuda_status(df::launch_conv_splitk(sp, maps, x, w.conv0, w.conv1, y, w.conv_part, p.M, p.H, p.T, p.NL,
+                                              p.raw ? 1 : 0, w.bar, w.err, s));
+  }
   if (p.bf16 && p.chain)
     return cuda_status(df::launch_conv_chain(p.chain_plan, x, conv_w, w.conv0, w.conv1, y, p.M, p.H, p.T, p.NL,
                                              p.raw ? 1 : 0, w.bar, w.err, s));

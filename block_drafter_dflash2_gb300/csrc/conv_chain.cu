@@ -15,11 +15,12 @@
 //      y[m][c] = a * x[m-1][c] + b * x[m][c] for the group's 16 channels, x[-1] = 0 at each
 //      block start, rounded to bf16 and written to the layer's output buffer;
 //   3. the row block's barrier (its CTAs need every channel of the next layer's input rows).
-// Variants (template flags): the block's input rows x are staged in shared memory by one bulk
-// copy after the barrier (kStageX, 16-row blocks), or read from L2 with .cg loads (which skip
-// the non-coherent L1: the buffers are rewritten between layers); the weight slice is staged
-// in shared memory by a bulk copy requested as soon as the previous layer's taps are done
-// (kStageW), or read from global memory after an L2 prefetch issued a layer ahead.
+// Variants (template flags): the block's input rows x are staged in shared memory by bulk
+// copies (one per row) after the barrier (kStageX, 16-row blocks), or read from L2 with .cg
+// loads (which skip the non-coherent L1: the buffers are rewritten between layers); the weight
+// slice is staged in shared memory by bulk copies requested as soon as the previous layer's
+// taps are done (kStageW), or read from global memory after an L2 prefetch issued a layer
+// ahead. Staged rows are padded by 64 bytes so the fragment loads are free of bank conflicts.
 // Barriers are atomic counters in the workspace (zeroed by the host before the launch) with
 // a bounded spin: on timeout the kernel sets DFLASH2_DEVERR_WAIT_TIMEOUT and stops.
 #include <cuda_bf16.h>
@@ -27,6 +28,7 @@
 
 #include "../../include/dflash2.h"
 #include "kernels.h"
+#include "grid_sync.cuh"
 #include "ptx.cuh"
 
 namespace df {
@@ -34,6 +36,7 @@ namespace df {
 namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+constexpr int kRowPad = 32;  // bf16 elements of padding per staged row
 
 DF_DEV void bulk_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -44,34 +47,6 @@ DF_DEV void bulk_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes, uint6
 
 DF_DEV void prefetch_l2(const void* gmem_src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gmem_src), "r"(bytes) : "memory");
-}
-
-DF_DEV uint32_t ld_acquire(const unsigned* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// Barrier number `round` (1, 2, ...) of `members` CTAs sharing `count`.
-DF_DEV bool group_barrier(unsigned* count, unsigned round, unsigned members, int32_t* err, volatile int* stop) {
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(count, 1u);
-    const unsigned target = round * members;
-    const uint64_t t0 = globaltimer_ns();
-    while (ld_acquire(count) < target) {
-      __nanosleep(32);
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
-        flag_error(err, DFLASH2_DEVERR_WAIT_TIMEOUT);
-        *stop = 1;
-        break;
-      }
-    }
-    __threadfence();
-  }
-  __syncthreads();
-  return *stop == 0;
 }
 
 // d += A(16x16 fragments a0..a3) * B(16x8 fragments b0, b1), bf16 in, fp32 out
@@ -98,6 +73,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int RB = 16 * kMT;          // rows per block
   constexpr int kSlices = kWarps / kMT;  // hidden slices per row tile
   constexpr int TQ = kNT * 8;            // taps per CTA, padded
+  constexpr int kAcc = kNT == 1 ? 4 : (kNT <= 3 ? 2 : 1);  // independent accumulator sets
   extern __shared__ __align__(128) uint8_t smem_raw[];
   __shared__ uint64_t wbar, xbar;
   __shared__ int stop;
@@ -109,12 +85,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int g1 = (int)((int64_t)(gb + 1) * G / GBn);
   const int ntaps = 2 * (g1 - g0);
   const uint32_t slice_bytes = (uint32_t)ntaps * H * 2;
+  // staged rows are kRowPad elements longer than H (a 64-byte step modulo 128), so the
+  // 16-byte fragment loads of lanes in different rows fall in different banks
+  const int xstride = kStageX ? H + kRowPad : H;
+  const int wstride = kStageW ? H + kRowPad : H;
   // shared memory: [weight slice (kStageW)] [x rows (kStageX)] [partial tiles] [taps]
   uint8_t* p = smem_raw;
   __nv_bfloat16* ws = reinterpret_cast<__nv_bfloat16*>(p);
-  if constexpr (kStageW) p += (size_t)wtaps * H * 2;
+  if constexpr (kStageW) p += (size_t)wtaps * (H + kRowPad) * 2;
   __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(p);
-  if constexpr (kStageX) p += (size_t)RB * H * 2;
+  if constexpr (kStageX) p += (size_t)RB * (H + kRowPad) * 2;
   float* red = reinterpret_cast<float*>(p);  // [kSlices][RB][TQ]
   p += (size_t)kSlices * RB * TQ * 4;
   float* taps_s = reinterpret_cast<float*>(p);  // [RB][TQ]
@@ -127,7 +107,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_barrier_init();
     if constexpr (kStageW) {
       mbar_arrive_expect_tx(&wbar, slice_bytes);
-      bulk_g2s(ws, W + (size_t)(2 * g0) * H, slice_bytes, &wbar);
+      for (int q = 0; q < ntaps; ++q) bulk_g2s(ws + (size_t)q * wstride, W + (size_t)(2 * g0 + q) * H, H * 2, &wbar);
     } else {
       prefetch_l2(W + (size_t)(2 * g0) * H, slice_bytes);
     }
@@ -150,12 +130,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!kStageW && tid == 0 && l + 1 < NL) prefetch_l2(wl + (size_t)P * H, slice_bytes);
     const __nv_bfloat16* xb = xin_g + (size_t)r0 * H;  // the block's first row
     if constexpr (kStageX) {
-      if (tid == 0) {
+      if (warp == 0) {
         // rows written by other CTAs' generic stores before the barrier; order them before
-        // this async-proxy read
+        // this async-proxy read. One bulk copy per row, spread over the lanes, so the rows
+        // stream in parallel.
+        if (lane == 0) mbar_arrive_expect_tx(&xbar, (uint32_t)nrows * H * 2);
+        __syncwarp();
         asm volatile("fence.proxy.async.global;" ::: "memory");
-        mbar_arrive_expect_tx(&xbar, (uint32_t)nrows * H * 2);
-        bulk_g2s(xs, xb, (uint32_t)nrows * H * 2, &xbar);
+        for (int m = lane; m < nrows; m += 32)
+          bulk_g2s(xs + (size_t)m * xstride, xb + (size_t)m * H, (uint32_t)H * 2, &xbar);
       }
       if (!mbar_wait(&xbar, xphase, err, &stop)) break;
       xphase ^= 1u;
@@ -170,37 +153,55 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- 1. taps
     {
-      float acc[kNT][4];
+      // kAcc independent accumulator sets (32-wide chunks c go to set c % kAcc), so the
+      // MMAs of consecutive chunks do not wait on each other; summed at the end
+      float acc[kAcc][kNT][4];
 #pragma unroll
-      for (int nt = 0; nt < kNT; ++nt)
+      for (int a = 0; a < kAcc; ++a)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+        for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[a][nt][e] = 0.f;
       bool tap_ok[kNT];
 #pragma unroll
       for (int nt = 0; nt < kNT; ++nt) tap_ok[nt] = nt * 8 + g < ntaps;
-#pragma unroll 2
-      for (int k0 = kbeg; k0 < kbeg + kw; k0 += 32) {
-        const int kk = k0 + 8 * j;
-        const uint4 xa = ld16<kStageX>(xa_base + (size_t)rlo * H + kk);
-        const uint4 xc = ld16<kStageX>(xa_base + (size_t)rhi * H + kk);
-        uint4 wv[kNT];
+      const int kend = kbeg + kw;
+      for (int k0 = kbeg; k0 < kend; k0 += 32 * kAcc) {
+        uint4 xa[kAcc], xc[kAcc], wv[kAcc][kNT];
 #pragma unroll
-        for (int nt = 0; nt < kNT; ++nt)
-          wv[nt] = tap_ok[nt] ? ld16<kStageW>(wb_base + (size_t)(nt * 8 + g) * H + kk) : make_uint4(0, 0, 0, 0);
+        for (int a = 0; a < kAcc; ++a) {
+          const int kk = min(k0 + 32 * a, kend - 32) + 8 * j;  // a chunk past the end repeats the last one
+          xa[a] = ld16<kStageX>(xa_base + (size_t)rlo * xstride + kk);
+          xc[a] = ld16<kStageX>(xa_base + (size_t)rhi * xstride + kk);
 #pragma unroll
-        for (int nt = 0; nt < kNT; ++nt) {
-          mma_16816(acc[nt], xa.x, xc.x, xa.y, xc.y, wv[nt].x, wv[nt].y);
-          mma_16816(acc[nt], xa.z, xc.z, xa.w, xc.w, wv[nt].z, wv[nt].w);
+          for (int nt = 0; nt < kNT; ++nt)
+            wv[a][nt] =
+                tap_ok[nt] ? ld16<kStageW>(wb_base + (size_t)(nt * 8 + g) * wstride + kk) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int a = 0; a < kAcc; ++a) {
+          if (k0 + 32 * a >= kend) break;  // (uniform) the repeated chunk is not accumulated
+#pragma unroll
+          for (int nt = 0; nt < kNT; ++nt) {
+            mma_16816(acc[a][nt], xa[a].x, xc[a].x, xa[a].y, xc[a].y, wv[a][nt].x, wv[a][nt].y);
+            mma_16816(acc[a][nt], xa[a].z, xc[a].z, xa[a].w, xc[a].w, wv[a][nt].z, wv[a][nt].w);
+          }
         }
       }
+#pragma unroll
+      for (int a = 1; a < kAcc; ++a)
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[0][nt][e] += acc[a][nt][e];
       // accumulator layout: acc[nt][0..1] = row mt*16+g, taps nt*8+2j, +1; [2..3] = row +8
       float* rw = red + (size_t)ks * RB * TQ;
 #pragma unroll
       for (int nt = 0; nt < kNT; ++nt) {
-        rw[(mt * 16 + g) * TQ + nt * 8 + 2 * j] = acc[nt][0];
-        rw[(mt * 16 + g) * TQ + nt * 8 + 2 * j + 1] = acc[nt][1];
-        rw[(mt * 16 + g + 8) * TQ + nt * 8 + 2 * j] = acc[nt][2];
-        rw[(mt * 16 + g + 8) * TQ + nt * 8 + 2 * j + 1] = acc[nt][3];
+        rw[(mt * 16 + g) * TQ + nt * 8 + 2 * j] = acc[0][nt][0];
+        rw[(mt * 16 + g) * TQ + nt * 8 + 2 * j + 1] = acc[0][nt][1];
+        rw[(mt * 16 + g + 8) * TQ + nt * 8 + 2 * j] = acc[0][nt][2];
+        rw[(mt * 16 + g + 8) * TQ + nt * 8 + 2 * j + 1] = acc[0][nt][3];
       }
       __syncthreads();
       for (int e = tid; e < nrows * TQ; e += kThreads) {
@@ -212,11 +213,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncthreads();
     }
     // the staged weight slice is free: request the next layer's
-    if (kStageW && tid == 0 && l + 1 < NL) {
+    if (kStageW && warp == 0 && l + 1 < NL) {
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&wbar, slice_bytes);
+        w_pending = true;
+      }
+      __syncwarp();
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive_expect_tx(&wbar, slice_bytes);
-      bulk_g2s(ws, wl + (size_t)P * H, slice_bytes, &wbar);
-      w_pending = true;
+      for (int q = lane; q < ntaps; q += 32)
+        bulk_g2s(ws + (size_t)q * wstride, wl + (size_t)(P + q) * H, H * 2, &wbar);
     }
 
     // ---- 2. mix: 16-byte pieces (8 channels) of the CTA's channels, every row of the block
@@ -237,10 +242,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         b = e1 * inv;
       }
       const int c0 = (g0 + jg) * 16 + (pc & 1) * 8;
-      const uint4 cur = ld16<kStageX>(xa_base + (size_t)m * H + c0);
+      const uint4 cur = ld16<kStageX>(xa_base + (size_t)m * xstride + c0);
       uint4 prv = make_uint4(0, 0, 0, 0);
       if ((r0 + m) % T != 0)  // the previous row of the same sequence (outside the block if m == 0)
-        prv = m > 0 ? ld16<kStageX>(xa_base + (size_t)(m - 1) * H + c0)
+        prv = m > 0 ? ld16<kStageX>(xa_base + (size_t)(m - 1) * xstride + c0)
                     : __ldcg(reinterpret_cast<const uint4*>(xb - H + c0));
       const __nv_bfloat162* c2 = reinterpret_cast<const __nv_bfloat162*>(&cur);
       const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&prv);
@@ -270,7 +275,8 @@ constexpr Variant kVariants[] = {{true, true, 1, 1}, {true, false, 1, 3}, {false
 
 size_t variant_smem(const Variant& v, int H, int wtaps) {
   const int RB = 16 * v.mt, slices = kWarps / v.mt, TQ = v.nt * 8;
-  return (v.sw ? (size_t)wtaps * H * 2 : 0) + (v.sx ? (size_t)RB * H * 2 : 0) + (size_t)slices * RB * TQ * 4 +
+  return (v.sw ? (size_t)wtaps * (H + kRowPad) * 2 : 0) + (v.sx ? (size_t)RB * (H + kRowPad) * 2 : 0) +
+         (size_t)slices * RB * TQ * 4 +
          (size_t)RB * TQ * 4;
 }
 

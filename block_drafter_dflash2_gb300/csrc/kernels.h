@@ -40,6 +40,26 @@ cudaError_t launch_conv_chain(const ConvChainPlan& pl, const void* x, const void
                               void* z, int M, int H, int T, int NL, int raw, unsigned* bar_counts, int32_t* err,
                               cudaStream_t s);
 
+// All conv layers in one cooperative launch for larger row counts (bf16, hidden % 64 == 0):
+// CTAs = row tiles (128 rows) x tap tiles x K-slices; tcgen05 partial taps per K-slice, summed
+// after a grid barrier and fused with the mix. conv_splitk_plan sizes the grid for the SM count
+// (false if the row tiles do not fit); part_bytes of workspace hold the partial taps.
+struct ConvSplitPlan {
+  int RT, NT, KS;      // row tiles, tap tiles, K-slices
+  int Nt;              // projection rows per tap tile
+  int a_tail_rows;     // TMA box rows of the last row tile
+  int Mp;              // rows of a partial-tap plane (M rounded up to 4)
+  int grid;            // RT * NT * KS CTAs
+  size_t smem;         // dynamic shared memory per CTA
+  size_t part_bytes;   // workspace for the partial taps
+};
+bool conv_splitk_plan(int M, int H, int NL, int sms, ConvSplitPlan* out);
+// maps: x (128-row box), x (tail box), buf0, buf0 tail, buf1, buf1 tail, all layers' weights
+// [NL * H/8, H] (Nt-row box). Zeroes the barrier counters first.
+cudaError_t launch_conv_splitk(const ConvSplitPlan& pl, const CUtensorMap* maps, const void* x, void* buf0,
+                               void* buf1, void* z, float* part, int M, int H, int T, int NL, int raw,
+                               unsigned* bar_counts, int32_t* err, cudaStream_t s);
+
 // fp32 instantiations (small sizes).
 cudaError_t launch_conv_layer_f32(const float* x, const float* w, float* y, int M, int H, int T, int raw,
                                   cudaStream_t s);

@@ -77,10 +77,11 @@ def test_fp32_small_rows():
 # ------------------------------------------------------------------ per-step calls
 
 
-# batch 5 (40 rows) runs the single-launch conv chain; batch 12 (96 rows) the per-layer
-# tensor-core path
-@pytest.mark.parametrize("layers,raw,batch", [(1, False, 5), (5, False, 5), (1, True, 5), (1, False, 12),
-                                              (5, False, 12), (1, True, 12)])
+# 8 and 16 rows run the chain kernel that reads whole rows per CTA; 40, 96 and 160 rows the
+# split-K chain (one row tile; one tile; two tiles with a 32-row tail)
+@pytest.mark.parametrize("layers,raw,batch", [(1, False, 1), (5, False, 1), (5, False, 2), (1, False, 5),
+                                              (5, False, 5), (1, True, 5), (1, False, 12), (5, False, 12),
+                                              (1, True, 12), (5, False, 20)])
 def test_conv_step(layers, raw, batch):
     rc = _recipe(batch=batch, block=8, hidden=5120, vocab=64, layers=layers)
     sh = rc.shape
@@ -103,6 +104,19 @@ def test_conv_step_block16_many_rows():
     z_ref = O.conv_chain(inp["hidden"], inp["conv_w"], "bf16", 16)
     z = P.run_conv(P.shape_of(sh), P.dev(inp["hidden"]), P.dev(inp["conv_w"]))
     P.check_conv(z, z_ref)
+
+
+@pytest.mark.parametrize("batch,block,hidden,layers", [(11, 12, 512, 3), (1, 8, 1088, 2), (4, 5, 1088, 2)])
+def test_conv_step_tile_edges(batch, block, hidden, layers):
+    # 132 rows with block 12: sequences cross the 128-row tile boundary and the last tile has
+    # 4 rows; hidden 1088 (not a multiple of 256) takes the per-layer path at 8 rows and the
+    # split-K chain at 20 rows of block 5, where 136 taps per layer fill a 144-row tap tile
+    rc = _recipe(batch=batch, block=block, hidden=hidden, vocab=64, layers=layers)
+    sh = rc.shape
+    inp = synth.make_inputs(rc)
+    z_ref = O.conv_chain(inp["hidden"], inp["conv_w"], "bf16", 16)
+    z = P.run_conv(P.shape_of(sh), P.dev(inp["hidden"]), P.dev(inp["conv_w"]))
+    print(P.check_conv(z, z_ref))
 
 
 def test_conv_shift_limit_exact():
