@@ -246,8 +246,11 @@ dflash2_status_t run_conv(const Plan& p, const void* x, const void* conv_w, void
 }
 
 dflash2_status_t run_partials(const Plan& p, const void* rows, const void* lm_head, const Ws& w, cudaStream_t s) {
-  // several row chunks share each column range: 256-column tiles halve the row-tile re-reads
-  TcGemmArgs a{p.M, p.H, p.V, p.n_rc, p.lm_parts, p.a_tail_rows, p.n_rc > 1 ? 16 : 8, p.lm_cluster, w.err};
+  // 256-column tiles once the row tile is not small: each stage's row-tile box is then shared
+  // by twice the weight columns (the copy engine issues box rows at a fixed rate; at 8 rows the
+  // stream is HBM-bound either way), and several row chunks re-read each row tile half as often
+  TcGemmArgs a{p.M, p.H, p.V, p.n_rc, p.lm_parts, p.a_tail_rows, (p.n_rc > 1 || p.M >= 32) ? 16 : 8,
+               p.lm_cluster, w.err};
   if (p.bf16) {
     CUtensorMap ma, mat, mb128, mb16;
     if (!encode_bf16_2d(&ma, rows, p.H, p.M, 128) || !encode_bf16_2d(&mat, rows, p.H, p.M, p.a_tail_rows) ||
