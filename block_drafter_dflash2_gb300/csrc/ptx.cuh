@@ -107,12 +107,16 @@ DF_DEV void tma_load_2d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, i
 
 // Same load, written to the same shared-memory offset of every CTA in `mask` (this CTA's
 // cluster), each destination's mbarrier at `bar`'s offset receiving the bytes it got.
+// The 16-bit CTA mask enters the asm as a 32-bit register and is narrowed inside it: handed
+// over as a 16-bit operand, it arrived with stray upper bits in some register allocations and
+// the copies never reached their CTAs.
 DF_DEV void tma_load_2d_mc(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int32_t c0, int32_t c1,
                            uint16_t mask, uint64_t policy) {
   asm volatile(
+      "{\n\t.reg .b16 m;\n\tcvt.u16.u32 m, %5;\n\t"
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(mask), "l"(policy)
+      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], m, %6;\n\t}" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"((uint32_t)mask), "l"(policy)
       : "memory");
 }
 
@@ -165,11 +169,14 @@ DF_DEV void umma_commit(uint64_t* bar) {
 
 // Arrive once on the mbarrier at `bar`'s offset in every CTA of `mask`, when every MMA issued
 // so far by this thread has completed.
+// (The mask is narrowed inside the asm, as for tma_load_2d_mc.)
 DF_DEV void umma_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::
-                   "r"(smem_u32(bar)),
-               "h"(mask)
-               : "memory");
+  asm volatile(
+      "{\n\t.reg .b16 m;\n\tcvt.u16.u32 m, %1;\n\t"
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], m;\n\t}" ::"r"(
+          smem_u32(bar)),
+      "r"((uint32_t)mask)
+      : "memory");
 }
 
 // Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, shape M x N.
