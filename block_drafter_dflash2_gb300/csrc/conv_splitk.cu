@@ -14,7 +14,8 @@
 //   grid barrier: every partial of the layer is written.
 //   B. The NT CTAs sharing (rt, ks) split the channel groups of the slice. For each of its
 //      (row, group) items a thread sums the group's two taps over the K-slices in slice
-//      order (16 slices loaded before any is added), normalises them (softmax over the pair, unless raw), and writes
+//      order (up to 20 slices loaded before any is added, the rows' channels issued
+//      first), normalises them (softmax over the pair, unless raw), and writes
 //      y[m, c] = a * x_l[m-1, c] + b * x_l[m, c] for the group's 16 channels (x[-1] = 0 at
 //      each block start), rounded to bf16.
 //   sibling barrier: the NT CTAs of (rt, ks) wait for each other, since the next layer's A
@@ -39,6 +40,7 @@ constexpr int kThreads = 256;
 constexpr int kStages = 5;
 constexpr uint32_t kABytes = 128 * 64 * 2;  // A region of a stage: the MMA reads 128 rows
 constexpr int kMaxTile = 160;                // widest tap tile
+constexpr int kC = 20;                       // K-slices whose partials a mix thread loads at once
 
 struct SplitArgs {
   int M, H, T, NL, raw;
@@ -224,21 +226,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = it % rows, gi = it / rows;
         const int g = g_lo + nt + gi * a.NT;
         const int row = rt * 128 + r;
+        const int c0 = g * 16;
+        // the rows' channels first, so their loads are in flight with the partials'
+        const uint4* cur = reinterpret_cast<const uint4*>(xin + (size_t)row * a.H + c0);
+        uint4 cv[2] = {__ldcg(cur), __ldcg(cur + 1)};
+        uint4 pv[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+        if (row % a.T != 0) {
+          pv[0] = __ldcg(cur - a.H / 8);  // the previous row
+          pv[1] = __ldcg(cur - a.H / 8 + 1);
+        }
         const float* p0 = part + (size_t)(2 * g) * a.Mp + row;
-        // the partials of 16 K-slices are loaded before any is added, so a chunk costs one
-        // L2 round trip; they are added in slice order
+        // the partials of up to kC K-slices are loaded before any is added (one L2 round trip
+        // for every plan up to kC slices); they are added in slice order
         float s0 = 0.f, s1 = 0.f;
-        for (int sb = 0; sb < a.KS; sb += 16) {
-          float v0[16], v1[16];
+        for (int sb = 0; sb < a.KS; sb += kC) {
+          float v0[kC], v1[kC];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
+          for (int j = 0; j < kC; ++j) {
             if (sb + j < a.KS) {
               v0[j] = __ldcg(p0 + (size_t)(sb + j) * sstride);
               v1[j] = __ldcg(p0 + (size_t)(sb + j) * sstride + a.Mp);
             }
           }
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
+          for (int j = 0; j < kC; ++j) {
             if (sb + j < a.KS) {
               s0 += v0[j];
               s1 += v1[j];
@@ -255,15 +266,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float inv = 1.f / (e0 + e1);
           wa = e0 * inv;
           wb = e1 * inv;
-        }
-        const int c0 = g * 16;
-        const uint4* cur = reinterpret_cast<const uint4*>(xin + (size_t)row * a.H + c0);
-        uint4 cv[2] = {__ldcg(cur), __ldcg(cur + 1)};
-        uint4 pv[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
-        if (row % a.T != 0) {
-          const uint4* prv = reinterpret_cast<const uint4*>(xin + (size_t)(row - 1) * a.H + c0);
-          pv[0] = __ldcg(prv);
-          pv[1] = __ldcg(prv + 1);
         }
         uint4 out[2];
         const __nv_bfloat162* c2 = reinterpret_cast<const __nv_bfloat162*>(cv);
