@@ -17,7 +17,6 @@ using df::TcGemmArgs;
 constexpr int kMaxDevices = 64;
 
 int g_sm_count[kMaxDevices];
-int g_clusters[kMaxDevices][9];  // resident LM-head clusters per cluster size (0 = not queried, -1 = none)
 std::once_flag g_encode_once;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -30,17 +29,6 @@ int sm_count() {
     g_sm_count[dev] = n;
   }
   return g_sm_count[dev];
-}
-
-// Resident clusters of `cluster` LM-head CTAs on the current device, cached.
-int max_clusters(int cluster) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices || cluster > 8) return 0;
-  if (g_clusters[dev][cluster] == 0) {
-    const int n = df::lmhead_max_active_clusters(cluster);
-    g_clusters[dev][cluster] = n > 0 ? n : -1;
-  }
-  return g_clusters[dev][cluster] > 0 ? g_clusters[dev][cluster] : 0;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
@@ -126,16 +114,12 @@ dflash2_status_t make_plan(const dflash2_shape_t* s, Plan& p) {
     p.a_tail_rows = (p.M % 128 == 0) ? 128 : ((p.M % 128 + 7) / 8) * 8;
     const int per = sms / p.n_rc > 0 ? sms / p.n_rc : 1;
     p.lm_parts = per < v_units ? per : v_units;
+    // No clusters: the row-chunk CTAs of a column range each load the whole weight tile and the
+    // second read of a tile mostly hits L2. Clusters that multicast each tile to the chunks
+    // (the kernel supports them) measured slower at every size, 2 % at 256 rows and 35 % at
+    // 512: a multicast stage completes only when every CTA's share has landed and is reused
+    // only when every CTA has released it, so one slow CTA stalls the others.
     p.lm_cluster = 1;
-    if (p.n_rc == 2 || p.n_rc == 4 || p.n_rc == 8) {
-      // the row chunks of a column range form a cluster and share its weight tiles; as many
-      // ranges as clusters fit on the device at once
-      const int nc = max_clusters(p.n_rc);
-      if (nc > 0) {
-        p.lm_cluster = p.n_rc;
-        p.lm_parts = nc < v_units ? nc : v_units;
-      }
-    }
     p.conv_parts = per < p_units ? per : p_units;
     p.split = p.M > kChainMaxRows && p.NL > 0 && df::conv_splitk_plan(p.M, p.H, p.NL, sms, &p.split_plan);
     p.chain = !p.split && df::conv_chain_plan(p.M, p.H, sms, &p.chain_plan);

@@ -15,10 +15,6 @@ cudaError_t launch_lmhead_topk_bf16(const CUtensorMap& a, const CUtensorMap& a_t
                                     const TcGemmArgs& args, float* part_val, int32_t* part_id,
                                     float* part_ms, cudaStream_t s);
 
-// How many clusters of `cluster` CTAs of the LM-head kernel can be resident at once on the
-// current device (0 if the query fails).
-int lmhead_max_active_clusters(int cluster);
-
 // tcgen05 GEMM + conv-layer epilogue (bf16): y = mix(x) with taps = x * W^T.
 cudaError_t launch_conv_layer_bf16(const CUtensorMap& a, const CUtensorMap& a_tail, const CUtensorMap& b128,
                                    const CUtensorMap& b16,

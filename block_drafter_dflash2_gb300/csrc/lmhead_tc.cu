@@ -42,31 +42,6 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& a_tail, const C
 }
 }  // namespace
 
-int lmhead_max_active_clusters(int cluster) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (cudaFuncSetAttribute(tc_gemm_kernel<EpiTopK>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes) !=
-      cudaSuccess)
-    return 0;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(cluster);
-  cfg.blockDim = dim3(kGemmThreads);
-  cfg.dynamicSmemBytes = kGemmSmemBytes;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cluster;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<EpiTopK>, &cfg) != cudaSuccess) {
-    cudaGetLastError();
-    return 0;
-  }
-  return n;
-}
-
 cudaError_t launch_lmhead_topk_bf16(const CUtensorMap& a, const CUtensorMap& a_tail, const CUtensorMap& b128,
                                     const CUtensorMap& b16, const TcGemmArgs& args, float* part_val,
                                     int32_t* part_id, float* part_ms, cudaStream_t s) {

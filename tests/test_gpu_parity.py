@@ -137,9 +137,9 @@ def test_conv_shift_limit_exact():
     assert np.array_equal(z, exp)
 
 
-# 256 and 512 rows run clusters whose row-chunk CTAs share each weight tile; the vocabularies
-# near 16 x 16 columns per range leave neighbouring ranges with different tile counts; 64 and 40
-# rows take 256-column tiles without clusters; 200 rows end in a ragged chunk
+# 256 and 512 rows run two and four 128-row chunks per column range; the vocabularies near 16 x 16
+# columns per range leave neighbouring ranges with different tile counts; 64 and 40 rows take
+# 256-column tiles in one chunk; 200 rows end in a ragged chunk
 @pytest.mark.parametrize("M,V,H", [(8, 248_320 // 8, 5120), (256, 30_011, 512), (1, 777, 64), (256, 16_400, 256),
                                    (256, 18_448, 256), (256, 19_472, 256), (512, 20_000, 256), (64, 9_001, 256),
                                    (40, 5_000, 256), (200, 12_345, 256)])
