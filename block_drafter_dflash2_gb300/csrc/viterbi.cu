@@ -60,6 +60,51 @@ __device__ __forceinline__ int32_t clamp_id(int32_t id, int vocab, int32_t* err,
   return id;
 }
 
+// 16 x 16 products of the rows staged in stA (16 x rc) and stB (16 x rc), accumulated into acc.
+__device__ __forceinline__ void tile_mma(const __nv_bfloat16* stA, const __nv_bfloat16* stB, int rc,
+                                         float (&acc)[2][4]) {
+  const int lane = threadIdx.x & 31;
+  for (int k0 = 0; k0 < rc; k0 += 16) {
+    uint32_t a[4], b[4];
+    {
+      const int r = (lane & 7) + ((lane >> 3) & 1) * 8;
+      const int c = k0 + (lane >> 4) * 8;
+      ldmatrix_x4(static_cast<uint32_t>(__cvta_generic_to_shared(stA + r * kRowPad + c)), a[0], a[1], a[2], a[3]);
+    }
+    {
+      const int n = (lane & 7) + (lane >> 4) * 8;
+      const int c = k0 + ((lane >> 3) & 1) * 8;
+      ldmatrix_x4(static_cast<uint32_t>(__cvta_generic_to_shared(stB + n * kRowPad + c)), b[0], b[1], b[2], b[3]);
+    }
+    mma_bf16_16816(acc[0], a, b[0], b[1]);
+    mma_bf16_16816(acc[1], a, b[2], b[3]);
+  }
+}
+
+__device__ __forceinline__ void store_tau(const float (&acc)[2][4], float (&tau)[kKP][kKP]) {
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, c2 = (lane & 3) * 2;
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    tau[g][nt * 8 + c2] = acc[nt][0];
+    tau[g][nt * 8 + c2 + 1] = acc[nt][1];
+    tau[g + 8][nt * 8 + c2] = acc[nt][2];
+    tau[g + 8][nt * 8 + c2 + 1] = acc[nt][3];
+  }
+}
+
+// Issues (without waiting) the 16-byte copies of rows ids[0..15] of E (R <= kRChunk columns)
+// into the 16 padded rows at st.
+__device__ __forceinline__ void gather_rows(const __nv_bfloat16* __restrict__ E, int R, const int32_t* ids,
+                                            __nv_bfloat16* st) {
+  const int lane = threadIdx.x & 31;
+  const int vec_per_row = R / 8;
+  for (int v = lane; v < kKP * vec_per_row; v += 32) {
+    const int row = v / vec_per_row, cv = v % vec_per_row;
+    cp_async16(st + row * kRowPad + cv * 8, E + (size_t)ids[row] * R + cv * 8);
+  }
+}
+
 // tau tile for one boundary, bf16 embeddings, on one warp.
 __device__ void tile_bf16(const __nv_bfloat16* __restrict__ U, const __nv_bfloat16* __restrict__ V, int R,
                           const int32_t* prev, const int32_t* cur, __nv_bfloat16* stA, __nv_bfloat16* stB,
@@ -79,30 +124,9 @@ __device__ void tile_bf16(const __nv_bfloat16* __restrict__ U, const __nv_bfloat
     cp_async_commit();
     cp_async_wait_all();
     __syncwarp();
-    for (int k0 = 0; k0 < rc; k0 += 16) {
-      uint32_t a[4], b[4];
-      {
-        const int r = (lane & 7) + ((lane >> 3) & 1) * 8;
-        const int c = k0 + (lane >> 4) * 8;
-        ldmatrix_x4(static_cast<uint32_t>(__cvta_generic_to_shared(stA + r * kRowPad + c)), a[0], a[1], a[2], a[3]);
-      }
-      {
-        const int n = (lane & 7) + (lane >> 4) * 8;
-        const int c = k0 + ((lane >> 3) & 1) * 8;
-        ldmatrix_x4(static_cast<uint32_t>(__cvta_generic_to_shared(stB + n * kRowPad + c)), b[0], b[1], b[2], b[3]);
-      }
-      mma_bf16_16816(acc[0], a, b[0], b[1]);
-      mma_bf16_16816(acc[1], a, b[2], b[3]);
-    }
+    tile_mma(stA, stB, rc, acc);
   }
-  const int g = lane >> 2, c2 = (lane & 3) * 2;
-#pragma unroll
-  for (int nt = 0; nt < 2; ++nt) {
-    tau[g][nt * 8 + c2] = acc[nt][0];
-    tau[g][nt * 8 + c2 + 1] = acc[nt][1];
-    tau[g + 8][nt * 8 + c2] = acc[nt][2];
-    tau[g + 8][nt * 8 + c2 + 1] = acc[nt][3];
-  }
+  store_tau(acc, tau);
 }
 
 // tau tile for one boundary, fp32 embeddings (small instantiation): 8 entries per lane.
@@ -267,6 +291,15 @@ __host__ __device__ inline size_t merge_stage_bytes(int parts) {
   return (((size_t)parts * 16 * 8 + (size_t)parts * 8 + (size_t)parts) + 127) & ~size_t(127);
 }
 
+// Per-warp region of the fused kernel: the merge staging of one row, later the gathered
+// V rows of its slot and the U rows that feed the next slot's tile.
+constexpr size_t kTileStageBytes = (size_t)2 * kKP * kRowPad * sizeof(__nv_bfloat16);
+constexpr size_t kAnchorStageBytes = (size_t)kKP * kRowPad * sizeof(__nv_bfloat16);
+__host__ __device__ inline size_t select_region_stride(int parts) {
+  const size_t m = merge_stage_bytes(parts);
+  return m > kTileStageBytes ? m : kTileStageBytes;
+}
+
 template <bool kBf16>
 __global__ void __launch_bounds__(32 * kWarps)
     select_walk_kernel(const float* __restrict__ part_val, const int32_t* __restrict__ part_id,
@@ -280,27 +313,49 @@ __global__ void __launch_bounds__(32 * kWarps)
   uint8_t* region = smem_raw + ((sizeof(SmemWalk) + 127) & ~size_t(127));
   const int b = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t wstride = select_region_stride(parts);
+  // One slot per warp and the rank in one staged chunk (the page shape): each warp gathers its
+  // slot's embedding rows as soon as its merge is done, while the other warps still merge, and
+  // the anchor's U row (tile 0's A operand, the same for all 16 rows) is fetched first.
+  const bool early = kBf16 && T <= kWarps && R <= kRChunk;
+  __nv_bfloat16* a0 = reinterpret_cast<__nv_bfloat16*>(region + kWarps * wstride);
 
-  if (threadIdx.x == 0) sw.anchor = clamp_id(anchor[b], vocab, err, DFLASH2_DEVERR_ANCHOR_RANGE);
+  if (warp == 0) {
+    int32_t anc = 0;
+    if (lane == 0) {
+      anc = clamp_id(anchor[b], vocab, err, DFLASH2_DEVERR_ANCHOR_RANGE);
+      sw.anchor = anc;
+    }
+    anc = __shfl_sync(0xffffffffu, anc, 0);
+    if (early) {
+      const __nv_bfloat16* U = reinterpret_cast<const __nv_bfloat16*>(Uv);
+      const int vec_per_row = R / 8;
+      for (int v = lane; v < kKP * vec_per_row; v += 32)
+        cp_async16(a0 + (v / vec_per_row) * kRowPad + (v % vec_per_row) * 8, U + (size_t)anc * R + (v % vec_per_row) * 8);
+      cp_async_commit();
+    }
+  }
   {
-    const size_t wbytes = merge_stage_bytes(parts);
-    float* sv = reinterpret_cast<float*>(region + warp * wbytes);
+    float* sv = reinterpret_cast<float*>(region + warp * wstride);
     int32_t* si = reinterpret_cast<int32_t*>(sv + parts * 16);
     float2* sms = reinterpret_cast<float2*>(si + parts * 16);
     uint8_t* head = reinterpret_cast<uint8_t*>(sms + parts);
     for (int t = warp; t < T; t += kWarps) {
       const int row = b * T + t;
+      // the row's lists and (max, sum) pairs in one batch of async copies
       for (int e = lane; e < parts * 4; e += 32) {
         const int p = e >> 2, q = e & 3;
         const size_t src = ((size_t)p * M + row) * 16 + q * 4;
         cp_async16(sv + e * 4, part_val + src);
         cp_async16(si + e * 4, part_id + src);
       }
-      cp_async_commit();
       for (int p = lane; p < parts; p += 32) {
-        sms[p] = part_ms[(size_t)p * M + row];
+        cp_async8(sms + p, part_ms + (size_t)p * M + row);
         head[p] = 0;
       }
+      cp_async_commit();
+      cp_async_wait_all();
+      __syncwarp();
       float m = -INFINITY;
       for (int p = lane; p < parts; p += 32) m = fmaxf(m, sms[p].x);
 #pragma unroll
@@ -312,8 +367,6 @@ __global__ void __launch_bounds__(32 * kWarps)
       for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
       const float lse = m + logf(s);
       if (lane == 0 && lse_out) lse_out[row] = lse;
-      cp_async_wait_all();
-      __syncwarp();
       warp_merge_lists(sv, si, head, parts, K, [&](int k, int32_t id, float v) {
         const float lp = v - lse;
         sw.ids[t][k] = id;
@@ -322,13 +375,40 @@ __global__ void __launch_bounds__(32 * kWarps)
         if (cand_lp) cand_lp[(size_t)row * K + k] = lp;
       });
       __syncwarp();
+      if (early) {
+        // pad the slot (as pad_candidates does) and start its gathers into this warp's
+        // region, whose merge staging is no longer needed: V rows for tile t, U rows for t+1
+        if (lane >= K && lane < kKP) {
+          sw.ids[t][lane] = sw.ids[t][0];
+          sw.lp[t][lane] = -INFINITY;
+        }
+        __syncwarp();
+        __nv_bfloat16* stB = reinterpret_cast<__nv_bfloat16*>(region + warp * wstride);
+        gather_rows(reinterpret_cast<const __nv_bfloat16*>(Vv), R, sw.ids[t], stB);
+        if (t + 1 < T) gather_rows(reinterpret_cast<const __nv_bfloat16*>(Uv), R, sw.ids[t], stB + kKP * kRowPad);
+        cp_async_commit();
+      }
     }
   }
-  __syncthreads();
-  pad_candidates(sw, T, K);
-  __syncthreads();
-  build_tiles<kBf16>(sw, T, R, Uv, Vv, reinterpret_cast<__nv_bfloat16*>(region));
-  __syncthreads();
+  if (early) {
+    cp_async_wait_all();
+    __syncthreads();  // every warp's gathers have landed
+    if (warp < T) {
+      const __nv_bfloat16* stA =
+          warp == 0 ? a0 : reinterpret_cast<const __nv_bfloat16*>(region + (warp - 1) * wstride) + kKP * kRowPad;
+      const __nv_bfloat16* stB = reinterpret_cast<const __nv_bfloat16*>(region + warp * wstride);
+      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      tile_mma(stA, stB, R, acc);
+      store_tau(acc, sw.tau[warp]);
+    }
+    __syncthreads();
+  } else {
+    __syncthreads();
+    pad_candidates(sw, T, K);
+    __syncthreads();
+    build_tiles<kBf16>(sw, T, R, Uv, Vv, reinterpret_cast<__nv_bfloat16*>(region));
+    __syncthreads();
+  }
   if (warp != 0) return;
   walk_warp0(sw, b, T, K, greedy, path_ids, path_idx, score);
 }
@@ -339,8 +419,7 @@ constexpr size_t kWalkStageBytes = (size_t)kWarps * 2 * kKP * kRowPad * sizeof(_
 
 size_t select_walk_smem(int parts) {
   const size_t base = (sizeof(SmemWalk) + 127) & ~size_t(127);
-  const size_t merge = (size_t)kWarps * merge_stage_bytes(parts);
-  return base + (merge > kWalkStageBytes ? merge : kWalkStageBytes);
+  return base + (size_t)kWarps * select_region_stride(parts) + kAnchorStageBytes;
 }
 
 cudaError_t launch_select_walk(bool bf16, const float* part_val, const int32_t* part_id, const float* part_ms,
