@@ -43,18 +43,47 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return g_encode;
 }
 
+// Encoded maps are cached per host thread (16 entries, round robin): a call re-encodes only
+// maps it has not seen with the same base, shape and box. Encoding costs microseconds of host
+// time per map, which an eager caller pays on every call.
+struct MapKey {
+  const void* base;
+  uint64_t inner, rows;
+  uint32_t box_rows;
+};
+struct MapCache {
+  MapKey key[16];
+  CUtensorMap map[16];
+  int n = 0, next = 0;
+};
+thread_local MapCache t_maps;
+
 // Row-major bf16 matrix [rows, inner] as a 2-D TMA map with a (64 x box_rows) box,
 // 128-byte swizzle, zero fill out of bounds.
 bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  for (int i = 0; i < t_maps.n; ++i) {
+    const MapKey& k = t_maps.key[i];
+    if (k.base == base && k.inner == inner && k.rows == rows && k.box_rows == box_rows) {
+      *map = t_maps.map[i];
+      return true;
+    }
+  }
   auto enc = encoder();
   if (!enc) return false;
   const cuuint64_t dims[2] = {inner, rows};
   const cuuint64_t strides[1] = {inner * 2};
   const cuuint32_t box[2] = {64, box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  if (enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  const int slot = t_maps.next;
+  t_maps.key[slot] = MapKey{base, inner, rows, box_rows};
+  t_maps.map[slot] = *map;
+  t_maps.next = (slot + 1) % 16;
+  if (t_maps.n < 16) ++t_maps.n;
+  return true;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

@@ -29,6 +29,7 @@
 #include "../../include/dflash2.h"
 #include "kernels.h"
 #include "grid_sync.cuh"
+#include "launch_util.h"
 #include "ptx.cuh"
 
 namespace df {
@@ -318,7 +319,8 @@ cudaError_t launch_conv_chain(const ConvChainPlan& pl, const void* x, const void
                         reinterpret_cast<const void*>(conv_chain_kernel<false, true, 4, 3>),
                         reinterpret_cast<const void*>(conv_chain_kernel<false, false, 4, 9>)};
   if (pl.variant < 0 || pl.variant > 3) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(fns[pl.variant], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+  static unsigned char smem_done[4][64];
+  cudaError_t e = smem_opt_in(fns[pl.variant], smem_done[pl.variant]);
   if (e != cudaSuccess) return e;
   e = cudaMemsetAsync(bar_counts, 0, sizeof(unsigned) * pl.row_blocks, s);
   if (e != cudaSuccess) return e;

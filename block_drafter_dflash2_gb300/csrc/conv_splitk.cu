@@ -31,6 +31,7 @@
 #include "../../include/dflash2.h"
 #include "grid_sync.cuh"
 #include "kernels.h"
+#include "launch_util.h"
 #include "ptx.cuh"
 
 namespace df {
@@ -333,7 +334,8 @@ bool conv_splitk_plan(int M, int H, int NL, int sms, ConvSplitPlan* out) {
 cudaError_t launch_conv_splitk(const ConvSplitPlan& pl, const CUtensorMap* maps, const void* x, void* buf0,
                                void* buf1, void* z, float* part, int M, int H, int T, int NL, int raw,
                                unsigned* bar_counts, int32_t* err, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(conv_splitk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+  static unsigned char smem_done[64];
+  cudaError_t e = smem_opt_in(reinterpret_cast<const void*>(conv_splitk_kernel), smem_done);
   if (e != cudaSuccess) return e;
   e = cudaMemsetAsync(bar_counts, 0, sizeof(unsigned) * (1 + (size_t)pl.RT * pl.KS), s);
   if (e != cudaSuccess) return e;

@@ -1,6 +1,7 @@
 // bf16 instantiations of the tcgen05 GEMM: LM head with the top-K/lse epilogue, and one
 // conv layer with the tap-mix epilogue.
 #include "kernels.h"
+#include "launch_util.h"
 #include "tc_gemm.cuh"
 
 namespace df {
@@ -10,15 +11,9 @@ template <class Epi>
 cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& a_tail, const CUtensorMap& b128,
                         const CUtensorMap& b16, const TcGemmArgs& args, const typename Epi::Params& ep,
                         cudaStream_t s) {
-  static int configured_for = -1;  // device ordinal the smem attribute was set for
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static unsigned char smem_done[64];
+  cudaError_t e = smem_opt_in(reinterpret_cast<const void*>(tc_gemm_kernel<Epi>), smem_done);
   if (e != cudaSuccess) return e;
-  if (configured_for != dev) {
-    e = cudaFuncSetAttribute(tc_gemm_kernel<Epi>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured_for = dev;
-  }
   const int grid = args.n_rc * args.parts;
   if (args.cluster <= 1) {
     tc_gemm_kernel<Epi><<<grid, kGemmThreads, kGemmSmemBytes, s>>>(a, a_tail, b128, b16, args, ep);

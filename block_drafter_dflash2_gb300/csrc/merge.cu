@@ -10,6 +10,7 @@
 #include <math.h>
 
 #include "kernels.h"
+#include "launch_util.h"
 #include "select.cuh"
 
 namespace df {
@@ -81,7 +82,8 @@ cudaError_t launch_topk_merge(const float* part_val, const int32_t* part_id, con
   if (parts > kMaxParts) return cudaErrorInvalidValue;
   const size_t smem = (size_t)parts * 16 * 8 + parts;
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static unsigned char smem_done[64];
+    cudaError_t e = smem_opt_in(reinterpret_cast<const void*>(topk_merge_kernel), smem_done);
     if (e != cudaSuccess) return e;
   }
   topk_merge_kernel<<<M, kThreads, smem, s>>>(reinterpret_cast<const float4*>(part_val),

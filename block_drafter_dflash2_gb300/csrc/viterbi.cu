@@ -19,6 +19,7 @@
 
 #include "../../include/dflash2.h"
 #include "kernels.h"
+#include "launch_util.h"
 #include "select.cuh"
 
 namespace df {
@@ -432,13 +433,15 @@ cudaError_t launch_select_walk(bool bf16, const float* part_val, const int32_t* 
   cudaError_t e;
   const float2* ms = reinterpret_cast<const float2*>(part_ms);
   if (bf16) {
-    e = cudaFuncSetAttribute(select_walk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static unsigned char smem_done[64];
+    e = smem_opt_in(reinterpret_cast<const void*>(select_walk_kernel<true>), smem_done);
     if (e != cudaSuccess) return e;
     select_walk_kernel<true><<<B, 32 * kWarps, smem, s>>>(part_val, part_id, ms, parts, M, anchor, U, V, T, K, R,
                                                            vocab, greedy, cand_ids, cand_lp, lse, path_ids,
                                                            path_idx, score, err);
   } else {
-    e = cudaFuncSetAttribute(select_walk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static unsigned char smem_done[64];
+    e = smem_opt_in(reinterpret_cast<const void*>(select_walk_kernel<false>), smem_done);
     if (e != cudaSuccess) return e;
     select_walk_kernel<false><<<B, 32 * kWarps, smem, s>>>(part_val, part_id, ms, parts, M, anchor, U, V, T, K, R,
                                                             vocab, greedy, cand_ids, cand_lp, lse, path_ids,
@@ -456,12 +459,14 @@ cudaError_t launch_transition_walk(bool bf16, const int32_t* anchor, const int32
   const size_t smem = base + (bf16 ? kWalkStageBytes : 0);
   cudaError_t e;
   if (bf16) {
-    e = cudaFuncSetAttribute(transition_walk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static unsigned char smem_done[64];
+    e = smem_opt_in(reinterpret_cast<const void*>(transition_walk_kernel<true>), smem_done);
     if (e != cudaSuccess) return e;
     transition_walk_kernel<true><<<B, 32 * kWarps, smem, s>>>(anchor, cand_ids, cand_lp, U, V, T, K, R, vocab,
                                                                greedy, path_ids, path_idx, score, err);
   } else {
-    e = cudaFuncSetAttribute(transition_walk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static unsigned char smem_done[64];
+    e = smem_opt_in(reinterpret_cast<const void*>(transition_walk_kernel<false>), smem_done);
     if (e != cudaSuccess) return e;
     transition_walk_kernel<false><<<B, 32 * kWarps, smem, s>>>(anchor, cand_ids, cand_lp, U, V, T, K, R, vocab,
                                                                 greedy, path_ids, path_idx, score, err);
