@@ -101,6 +101,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* taps_s = reinterpret_cast<float*>(p);  // [RB][TQ]
   unsigned* my_bar = bar_counts + rb;
 
+  pdl_launch_dependents();  // the LM head may start its prologue as SMs free up
   if (tid == 0) {
     stop = 0;
     mbar_init(&wbar, 1);

@@ -98,6 +98,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t idesc = idesc_bf16_f32(128, a.Nt);
   const size_t part_layer = (size_t)a.KS * a.P * a.Mp;
 
+  pdl_launch_dependents();  // the LM head may start its prologue as SMs free up
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);

@@ -230,6 +230,15 @@ DF_DEV void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// ---------------------------------------------------------------- dependent launch
+
+// Lets the next kernel in the stream, if launched as a programmatic dependent, start its
+// prologue once every CTA of this grid has executed this (or exited).
+DF_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// Waits until the grids this one depends on have completed and their writes are visible;
+// returns at once for a kernel not launched as a programmatic dependent.
+DF_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- misc
 
 DF_DEV float ex2_approx(float x) {

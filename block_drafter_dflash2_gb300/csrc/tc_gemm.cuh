@@ -105,6 +105,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int CL = args.cluster;
   const uint16_t cl_mask = (uint16_t)((1u << CL) - 1u);
   const int crank = CL > 1 ? (int)cluster_ctarank() : 0;
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < sg.stages; ++s) {
       mbar_init(&full[s], 1);
@@ -139,6 +140,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint64_t pol_a = l2_policy_evict_last();   // row tiles are re-read for every column tile
       const uint64_t pol_b = l2_policy_evict_first();  // column tiles (weights) stream through once
       const CUtensorMap* ma = tail_chunk ? &map_a_tail : &map_a;
+      // The rows are the previous kernel's output (launched as its programmatic dependent,
+      // this kernel's prologue overlaps its end): wait for it before the first load.
+      pdl_wait();
       int stage = 0;
       uint32_t phase = 0;
       uint64_t issued = 0, issued_phase = 0;  // per-stage bits: ever issued / parity of last issue

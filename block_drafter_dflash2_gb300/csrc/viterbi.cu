@@ -20,6 +20,7 @@
 #include "../../include/dflash2.h"
 #include "kernels.h"
 #include "launch_util.h"
+#include "ptx.cuh"
 #include "select.cuh"
 
 namespace df {
@@ -336,6 +337,9 @@ __global__ void __launch_bounds__(32 * kWarps)
       cp_async_commit();
     }
   }
+  // the partials are the LM head's output (launched as its programmatic dependent, the
+  // prologue above overlaps its end)
+  pdl_wait();
   {
     float* sv = reinterpret_cast<float*>(region + warp * wstride);
     int32_t* si = reinterpret_cast<int32_t*>(sv + parts * 16);
@@ -432,20 +436,31 @@ cudaError_t launch_select_walk(bool bf16, const float* part_val, const int32_t* 
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
   cudaError_t e;
   const float2* ms = reinterpret_cast<const float2*>(part_ms);
+  // a programmatic dependent of the LM head: it reads the partials after griddepcontrol.wait
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(B);
+  cfg.blockDim = dim3(32 * kWarps);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (bf16) {
     static unsigned char smem_done[64];
     e = smem_opt_in(reinterpret_cast<const void*>(select_walk_kernel<true>), smem_done);
     if (e != cudaSuccess) return e;
-    select_walk_kernel<true><<<B, 32 * kWarps, smem, s>>>(part_val, part_id, ms, parts, M, anchor, U, V, T, K, R,
-                                                           vocab, greedy, cand_ids, cand_lp, lse, path_ids,
-                                                           path_idx, score, err);
+    e = cudaLaunchKernelEx(&cfg, select_walk_kernel<true>, part_val, part_id, ms, parts, M, anchor, U, V, T, K, R,
+                           vocab, greedy, cand_ids, cand_lp, lse, path_ids, path_idx, score, err);
+    if (e != cudaSuccess) return e;
   } else {
     static unsigned char smem_done[64];
     e = smem_opt_in(reinterpret_cast<const void*>(select_walk_kernel<false>), smem_done);
     if (e != cudaSuccess) return e;
-    select_walk_kernel<false><<<B, 32 * kWarps, smem, s>>>(part_val, part_id, ms, parts, M, anchor, U, V, T, K, R,
-                                                            vocab, greedy, cand_ids, cand_lp, lse, path_ids,
-                                                            path_idx, score, err);
+    e = cudaLaunchKernelEx(&cfg, select_walk_kernel<false>, part_val, part_id, ms, parts, M, anchor, U, V, T, K,
+                           R, vocab, greedy, cand_ids, cand_lp, lse, path_ids, path_idx, score, err);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }
