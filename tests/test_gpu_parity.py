@@ -106,6 +106,23 @@ def test_conv_step_block16_many_rows():
     P.check_conv(z, z_ref)
 
 
+# at most 8 rows in the chain kernel: sequences shorter than the rows (a sequence start inside
+# the row block), fewer channel groups than SMs (one group per CTA), raw taps, one row
+@pytest.mark.parametrize("batch,block,hidden,layers,raw", [(2, 4, 5120, 5, False), (1, 3, 1024, 3, False),
+                                                           (1, 8, 5120, 2, True), (4, 2, 256, 4, False),
+                                                           (1, 1, 512, 1, False)])
+def test_conv_step_few_rows(batch, block, hidden, layers, raw):
+    rc = _recipe(batch=batch, block=block, hidden=hidden, vocab=64, layers=layers)
+    sh = rc.shape
+    if raw:
+        sh.taps = "raw"
+        rc.conv_std = 0.002
+    inp = synth.make_inputs(rc)
+    z_ref = O.conv_chain(inp["hidden"], inp["conv_w"], "bf16", 16, sh.taps)
+    z = P.run_conv(P.shape_of(sh), P.dev(inp["hidden"]), P.dev(inp["conv_w"]))
+    print(P.check_conv(z, z_ref, x_in=inp["hidden"] if layers == 1 else None))
+
+
 @pytest.mark.parametrize("batch,block,hidden,layers", [(11, 12, 512, 3), (1, 8, 1088, 2), (4, 5, 1088, 2)])
 def test_conv_step_tile_edges(batch, block, hidden, layers):
     # 132 rows with block 12: sequences cross the 128-row tile boundary and the last tile has
@@ -119,9 +136,11 @@ def test_conv_step_tile_edges(batch, block, hidden, layers):
     print(P.check_conv(z, z_ref))
 
 
-def test_conv_shift_limit_exact():
-    # tap 0 dominant everywhere: z[t] = x[t - layers] exactly (the oracle's pinned special case)
-    B, T, H, L = 2, 8, 256, 3
+@pytest.mark.parametrize("B", [1, 2])
+def test_conv_shift_limit_exact(B):
+    # tap 0 dominant everywhere: z[t] = x[t - layers] exactly (the oracle's pinned special case),
+    # for one and two sequences in the row block
+    T, H, L = 8, 256, 3
     rng = np.random.default_rng(0)
     x = (rng.integers(1, 32, size=(B, T, H)) / 4.0).astype(np.float32)
     xb = (x.view(np.uint32) >> 16).astype(np.uint16)
