@@ -33,7 +33,11 @@ Readings where the pages are silent (each is a fixed choice, stated where used):
   R6 all `block` rows are slots; the anchor is the predecessor of slot 0.
   R7 per-slot score = log-softmax of the head's logits (this library's contract); the
      pages' raw-logit score gives the same path (per-slot constants cancel).
-  R8 the context gate H(h_t) is taken as all-ones.
+  R8 the context gate H(h_t) is taken as all-ones by default; with the gate on, H is a
+     linear map of the slot's hidden row with no nonlinearity (the pages give none):
+     g_t[r] = sum_h z_t[h] * gate_w[r, h], z_t = the slot's conv output (the row the LM
+     head reads), gate_w [R, H]. The selector's +2.0M parameters of Table 2 fit one such
+     [hidden x 256] map per embedding (3 x 2560 x 256 at the 4B target's hidden 2560).
   R9 the walk is a Viterbi (exact best path); the pages' greedy walk is kept as
      ``greedy_walk`` for comparison.
   R10 top-K order: logit descending, ties to the lower token id; Viterbi ties go
@@ -200,11 +204,19 @@ def cand_logprob(vals32: np.ndarray, lse: np.ndarray) -> np.ndarray:
 # ---------------------------------------------------------------------------
 
 
-def transitions(anchor: np.ndarray, cand_ids: np.ndarray, U: np.ndarray, V: np.ndarray) -> np.ndarray:
-    """tau [B, T, K, K] fp32. tau[b, 0, i, j] = <U[anchor_b], V[c_{b,0,j}]> for every i
-    (slot 0's predecessor is the anchor, R6); tau[b, t, i, j] = <U[c_{b,t-1,i}], V[c_{b,t,j}]>.
-    U embeds the previous token, V the current one (the pages' A and B, gate = 1, R8).
-    float64 dot products rounded once to fp32."""
+def context_gate(z_rows: np.ndarray, gate_w: np.ndarray) -> np.ndarray:
+    """The context gate H(h_t) of every slot row (R8): g[m, r] = sum_h z[m, h] * gate_w[r, h],
+    float64 dot products of the stored inputs, rounded once to fp32. z_rows [M, H], gate_w [R, H]."""
+    return (widen(z_rows) @ widen(gate_w).T).astype(np.float32)
+
+
+def transitions(anchor: np.ndarray, cand_ids: np.ndarray, U: np.ndarray, V: np.ndarray,
+                gate: np.ndarray | None = None) -> np.ndarray:
+    """tau [B, T, K, K] fp32. tau[b, 0, i, j] = <U[anchor_b] (.) g_{b,0}, V[c_{b,0,j}]> for every i
+    (slot 0's predecessor is the anchor, R6); tau[b, t, i, j] = <U[c_{b,t-1,i}] (.) g_{b,t}, V[c_{b,t,j}]>,
+    the pages' <A(a) (.) H(h_t), B(b)> with U = A (previous token) and V = B (current token);
+    g_{b,t} = gate[b, t] [R], the gate of the current slot t, or all-ones when gate is None (R8).
+    float64 sums of the triple products, rounded once to fp32."""
     B, T, K = cand_ids.shape
     Uw = widen(U)
     Vw = widen(V)
@@ -213,7 +225,10 @@ def transitions(anchor: np.ndarray, cand_ids: np.ndarray, U: np.ndarray, V: np.n
         prev = np.repeat(np.asarray([anchor[b]]), K)
         for t in range(T):
             cur = cand_ids[b, t]
-            tau[b, t] = (Uw[prev] @ Vw[cur].T).astype(np.float32)
+            a = Uw[prev]
+            if gate is not None:
+                a = a * np.asarray(gate[b, t], dtype=np.float64)[None, :]
+            tau[b, t] = (a @ Vw[cur].T).astype(np.float32)
             prev = cur
     return tau
 
@@ -372,12 +387,13 @@ def select_from_z(z: np.ndarray, inp: dict, shape, seqs, row_block: int = 64) ->
         lmax[r0:r0 + row_block] = l32.max(axis=1)
     lp = cand_logprob(vals, lse).reshape(nb, T, K)
     cids = ids.reshape(nb, T, K)
-    tau = transitions(anchor, cids, inp["U"], inp["V"])
+    gate = context_gate(rows, inp["gate_w"]).reshape(nb, T, -1) if getattr(shape, "gate", False) else None
+    tau = transitions(anchor, cids, inp["U"], inp["V"], gate)
     path_idx, score = viterbi(lp, tau)
     path_ids = np.take_along_axis(cids, path_idx[..., None].astype(np.int64), axis=2)[..., 0]
     best, second = viterbi_two_best(lp, tau)
     return dict(z=np.asarray(z), cand_ids=cids, cand_lp=lp, cand_logit=vals.reshape(nb, T, K),
                 next_logit=nxt.reshape(nb, T), max_logit=lmax.reshape(nb, T),
                 lse=lse.reshape(nb, T), lse32=lse.astype(np.float32).reshape(nb, T),
-                tau=tau, path_idx=path_idx, path_ids=path_ids.astype(np.int32), score=score,
+                tau=tau, gate=gate, path_idx=path_idx, path_ids=path_ids.astype(np.int32), score=score,
                 best=best, second=second, seqs=np.asarray(seqs))

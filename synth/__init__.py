@@ -34,6 +34,7 @@ TID_ANCHOR = 32
 TID_ANCHOR_DUP = 33
 TID_PLANT_ID = 34
 TID_PLANT_ON = 35
+TID_GATE_W = 36
 
 
 def build(force: bool = False) -> str:
@@ -140,6 +141,7 @@ class Shape:
     layers: int = 5
     dtype: str = "bf16"  # 'bf16' or 'f32'
     taps: str = "softmax"  # 'softmax' (default) or 'raw'
+    gate: bool = False     # context gate H(h_t) in the transition scores
 
     @property
     def rows(self) -> int:
@@ -160,6 +162,7 @@ class Recipe:
     lm_head_std: float = 0.02
     uv_std: float = 0.05
     conv_std: float = 0.02
+    gate_std: float = 0.0  # 0: 1 / sqrt(hidden), so a gate entry of a unit-rms row is about N(0, 1)
     plant: str = "none"  # 'none', 'all' (every slot, 1 % left unplanted), 'even_seq' (even sequences)
     plant_beta: float = 0.0
     anchor_dup_frac: float = 0.0
@@ -205,7 +208,8 @@ def make_inputs(rc: Recipe, with_lm_head: bool = True) -> dict:
     """Generate every input tensor of one workload.
 
     Returns numpy arrays: ``hidden`` [B,T,H], ``lm_head`` [V,H], ``U``/``V`` [V,R],
-    ``conv_w`` [NL,P,H] (bf16 bit patterns as uint16, or float32 for dtype f32) and
+    ``conv_w`` [NL,P,H], ``gate_w`` [R,H] (bf16 bit patterns as uint16, or float32 for
+    dtype f32) and
     ``anchor`` [B] int32, plus ``planted`` [B,T] int32 (-1 where a slot is not planted).
     """
     sh = rc.shape
@@ -217,6 +221,8 @@ def make_inputs(rc: Recipe, with_lm_head: bool = True) -> dict:
     out["lm_head"] = normal(s, TID_LM_HEAD, (Vv, H), rc.lm_head_std, kind) if with_lm_head else None
     out["U"] = normal(s, TID_U, (Vv, R), rc.uv_std, kind)
     out["V"] = normal(s, TID_V, (Vv, R), rc.uv_std, kind)
+    gate_std = rc.gate_std if rc.gate_std > 0 else 1.0 / np.sqrt(H)
+    out["gate_w"] = normal(s, TID_GATE_W, (R, H), gate_std, kind)
     out["conv_w"] = np.stack([normal(s, TID_CONV_W + l, (P, H), rc.conv_std, kind) for l in range(NL)]) \
         if NL > 0 else np.zeros((0, P, H), dtype=np.uint16 if kind == "bf16" else np.float32)
 

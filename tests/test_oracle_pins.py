@@ -230,6 +230,84 @@ def test_transitions_roles_of_u_and_v():
                     assert tau[b, t, i, j] == exp
 
 
+# ---------------------------------------------------------------- context gate
+
+
+def test_context_gate_hand_case():
+    # g[m, r] = sum_h z[m, h] gate_w[r, h] with small integers (exact in bf16 and fp32)
+    z = bf16_of([[1.0, 2.0, 3.0], [0.0, -1.0, 4.0]])
+    gw = bf16_of([[1.0, 0.0, 1.0], [2.0, 1.0, -1.0]])
+    g = O.context_gate(z, gw)
+    assert g.dtype == np.float32
+    assert np.array_equal(g, np.array([[4.0, 1.0], [4.0, -5.0]], np.float32))
+
+
+def _gate_case(seed=9, R=16, Vv=40, B=2, T=3, K=4):
+    rng = np.random.default_rng(seed)
+    U = bf16_of(np.round(rng.normal(size=(Vv, R)) * 8) / 8)
+    V = bf16_of(np.round(rng.normal(size=(Vv, R)) * 8) / 8)
+    cand = rng.integers(0, Vv, size=(B, T, K)).astype(np.int32)
+    anchor = rng.integers(0, Vv, size=B).astype(np.int32)
+    return U, V, cand, anchor, rng
+
+
+def test_gate_of_ones_is_the_ungated_score():
+    # <A(a) (.) 1, B(b)> = <A(a), B(b)>: the gate of all ones reproduces the ungated tiles bit for bit
+    U, V, cand, anchor, _ = _gate_case()
+    B, T, _ = cand.shape
+    ones = np.ones((B, T, U.shape[1]), np.float32)
+    assert np.array_equal(O.transitions(anchor, cand, U, V, ones), O.transitions(anchor, cand, U, V))
+
+
+def test_gate_one_hot_selects_one_embedding_dimension():
+    # gate = e_r: tau(i, j) = U[prev_i, r] * V[cur_j, r], the gate "decides which part of the match counts"
+    U, V, cand, anchor, _ = _gate_case()
+    B, T, K = cand.shape
+    R = U.shape[1]
+    r = 5
+    gate = np.zeros((B, T, R), np.float32)
+    gate[:, :, r] = 1.0
+    tau = O.transitions(anchor, cand, U, V, gate)
+    Uw, Vw = O.widen(U), O.widen(V)
+    for b in range(B):
+        for t in range(T):
+            for i in range(K):
+                prev = anchor[b] if t == 0 else cand[b, t - 1, i]
+                for j in range(K):
+                    assert tau[b, t, i, j] == np.float32(Uw[prev, r] * Vw[cand[b, t, j], r])
+
+
+def test_gate_is_the_current_slots_and_linear():
+    # the gate of slot t scales boundary t only (t-1 -> t), and tau is linear in it: g -> -2 g gives -2 tau
+    U, V, cand, anchor, rng = _gate_case()
+    B, T, _ = cand.shape
+    R = U.shape[1]
+    gate = (np.round(rng.normal(size=(B, T, R)) * 4) / 4).astype(np.float32)
+    tau = O.transitions(anchor, cand, U, V, gate)
+    assert np.array_equal(O.transitions(anchor, cand, U, V, -2.0 * gate), -2.0 * tau)
+    g2 = gate.copy()
+    g2[:, 1] = 0.0
+    tau2 = O.transitions(anchor, cand, U, V, g2)
+    assert np.all(tau2[:, 1] == 0.0)
+    assert np.array_equal(tau2[:, [0, 2]], tau[:, [0, 2]])
+
+
+def test_gated_tiny_workload_walk_is_brute_force_best():
+    rc = synth.recipe(1)
+    sh = rc.shape
+    sh.gate = True
+    inp = synth.make_inputs(rc)
+    out = O.draft_tail(inp, sh)
+    assert out["gate"] is not None and out["gate"].shape == (sh.batch, sh.block, sh.rank)
+    # the gate is H(h_t) of the slot's conv output row
+    z = out["z"].reshape(-1, sh.hidden)
+    g_direct = O.widen(z) @ O.widen(inp["gate_w"]).T
+    assert np.allclose(out["gate"].reshape(-1, sh.rank), g_direct, rtol=1e-6, atol=1e-6)
+    bp, bs = O.brute_force_best(out["cand_lp"], out["tau"])
+    assert np.array_equal(bp, out["path_idx"])
+    assert np.allclose(bs, out["score"], atol=1e-5)
+
+
 # ---------------------------------------------------------------- Viterbi
 
 
