@@ -95,6 +95,13 @@ def load(path: str = LIB_PATH):
     lib.dflash2_viterbi.restype = st
     lib.dflash2_draft_tail.argtypes = [sp, vp, vp, vp, vp, vp, i32p, i32p, i32p, vp, i32p, vp, vp, vp, sz, vp]
     lib.dflash2_draft_tail.restype = st
+    lib.dflash2_select_topk_gated.argtypes = [sp, vp, vp, vp, i32p, vp, vp, vp, vp, sz, vp]
+    lib.dflash2_select_topk_gated.restype = st
+    lib.dflash2_viterbi_gated.argtypes = [sp, i32p, i32p, vp, vp, vp, vp, i32p, i32p, vp, vp, sz, vp]
+    lib.dflash2_viterbi_gated.restype = st
+    lib.dflash2_draft_tail_gated.argtypes = [sp, vp, vp, vp, vp, vp, vp, i32p, i32p, i32p, vp, i32p, vp, vp, vp,
+                                             vp, sz, vp]
+    lib.dflash2_draft_tail_gated.restype = st
     lib.dflash2_read_device_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]
     lib.dflash2_read_device_error.restype = st
     lib.dflash2_status_string.argtypes = [st]
@@ -206,6 +213,32 @@ def draft_tail(shape: Shape, hidden, lm_head, U, V, conv_w, anchor, path_ids, pa
                                      _ptr(conv_w), _ptr(anchor), _ptr(path_ids), _ptr(path_idx), _ptr(score),
                                      _ptr(cand_ids), _ptr(cand_lp), _ptr(lse), wp, wn, _stream(stream)),
            "dflash2_draft_tail")
+
+
+def select_topk_gated(shape: Shape, rows, lm_head, gate_w, cand_ids, cand_lp, lse, gate, ws, stream=None):
+    """dflash2_select_topk_gated: select_topk plus the context gate rows . gate_w [R,H] -> gate [M,R]."""
+    wp, wn = _ws(ws)
+    _check(load().dflash2_select_topk_gated(ctypes.byref(shape), _ptr(rows), _ptr(lm_head), _ptr(gate_w),
+                                            _ptr(cand_ids), _ptr(cand_lp), _ptr(lse), _ptr(gate), wp, wn,
+                                            _stream(stream)), "dflash2_select_topk_gated")
+
+
+def viterbi_gated(shape: Shape, anchor, cand_ids, cand_lp, U, V, gate, path_ids, path_idx, score, ws, stream=None):
+    """dflash2_viterbi_gated: transitions U (.) gate_t against V, and the walk from the anchor."""
+    wp, wn = _ws(ws)
+    _check(load().dflash2_viterbi_gated(ctypes.byref(shape), _ptr(anchor), _ptr(cand_ids), _ptr(cand_lp), _ptr(U),
+                                        _ptr(V), _ptr(gate), _ptr(path_ids), _ptr(path_idx), _ptr(score), wp, wn,
+                                        _stream(stream)), "dflash2_viterbi_gated")
+
+
+def draft_tail_gated(shape: Shape, hidden, lm_head, U, V, conv_w, gate_w, anchor, path_ids, path_idx, score, ws,
+                     cand_ids=None, cand_lp=None, lse=None, gate=None, stream=None):
+    """dflash2_draft_tail_gated: the whole tail with the context gate (gate [B,T,R] optional out)."""
+    wp, wn = _ws(ws)
+    _check(load().dflash2_draft_tail_gated(ctypes.byref(shape), _ptr(hidden), _ptr(lm_head), _ptr(U), _ptr(V),
+                                           _ptr(conv_w), _ptr(gate_w), _ptr(anchor), _ptr(path_ids),
+                                           _ptr(path_idx), _ptr(score), _ptr(cand_ids), _ptr(cand_lp), _ptr(lse),
+                                           _ptr(gate), wp, wn, _stream(stream)), "dflash2_draft_tail_gated")
 
 
 def read_device_error(ws, stream=None) -> int:

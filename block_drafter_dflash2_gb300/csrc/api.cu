@@ -179,6 +179,7 @@ struct Ws {
   int32_t* cand_ids;
   float* cand_lp;
   float* lse;
+  float* gate;  // [M, R] fp32 context gate of the gated tail
   size_t total;
 };
 
@@ -201,6 +202,7 @@ Ws carve(const Plan& p, void* base) {
   w.part_ms = static_cast<float*>(take((size_t)p.lm_parts * p.M * 2 * 4));
   w.cand_ids = static_cast<int32_t*>(take((size_t)p.M * p.K * 4));
   w.cand_lp = static_cast<float*>(take((size_t)p.M * p.K * 4));
+  w.gate = static_cast<float*>(take((size_t)p.M * p.R * 4));
   w.lse = static_cast<float*>(take((size_t)p.M * 4));
   w.total = off;
   return w;
@@ -258,18 +260,33 @@ dflash2_status_t run_conv(const Plan& p, const void* x, const void* conv_w, void
   return DFLASH2_OK;
 }
 
-dflash2_status_t run_partials(const Plan& p, const void* rows, const void* lm_head, const Ws& w, cudaStream_t s) {
+// gate_w [R, H] (bf16; nullptr: no gate): the context gate's weights, contracted with the rows
+// in the same pass as gate columns past the vocabulary; gate_out [M, R] fp32 receives them.
+dflash2_status_t run_partials(const Plan& p, const void* rows, const void* lm_head, const Ws& w, cudaStream_t s,
+                              const void* gate_w = nullptr, float* gate_out = nullptr) {
   // 256-column tiles once the row tile is not small: each stage's row-tile box is then shared
   // by twice the weight columns (the copy engine issues box rows at a fixed rate; at 8 rows the
   // stream is HBM-bound either way), and several row chunks re-read each row tile half as often
   TcGemmArgs a{p.M, p.H, p.V, p.n_rc, p.lm_parts, p.a_tail_rows, (p.n_rc > 1 || p.M >= 32) ? 16 : 8,
                p.lm_cluster, w.err};
+  if (gate_w) {
+    if (!p.bf16 || !gate_out) return DFLASH2_ERR_UNSUPPORTED;
+    a.gate_base = (p.V + 15) / 16 * 16;
+    a.gate_cols = p.R;
+    a.n_total = a.gate_base + p.R;
+  }
   if (p.bf16) {
-    CUtensorMap ma, mat, mb128, mb16;
+    CUtensorMap ma, mat, mb128, mb16, mg16;
     if (!encode_bf16_2d(&ma, rows, p.H, p.M, 128) || !encode_bf16_2d(&mat, rows, p.H, p.M, p.a_tail_rows) ||
         !encode_bf16_2d(&mb128, lm_head, p.H, p.V, 128) || !encode_bf16_2d(&mb16, lm_head, p.H, p.V, 16))
       return DFLASH2_ERR_CUDA;
-    if (df::launch_lmhead_topk_bf16(ma, mat, mb128, mb16, a, w.part_val, w.part_id, w.part_ms, s) != cudaSuccess)
+    if (gate_w) {
+      if (!encode_bf16_2d(&mg16, gate_w, p.H, p.R, 16)) return DFLASH2_ERR_CUDA;
+    } else {
+      mg16 = mb16;
+    }
+    if (df::launch_lmhead_topk_bf16(ma, mat, mb128, mb16, mg16, a, p.V, w.part_val, w.part_id, w.part_ms,
+                                    gate_w ? gate_out : nullptr, s) != cudaSuccess)
       return DFLASH2_ERR_CUDA;
   } else {
     if (df::launch_lmhead_topk_f32(static_cast<const float*>(rows), static_cast<const float*>(lm_head), a,
@@ -284,17 +301,10 @@ dflash2_status_t run_merge(const Plan& p, int32_t* ids, float* lp, float* lse, c
       df::launch_topk_merge(w.part_val, w.part_id, w.part_ms, p.lm_parts, p.M, p.K, ids, lp, lse ? lse : w.lse, s));
 }
 
-dflash2_status_t run_topk(const Plan& p, const void* rows, const void* lm_head, int32_t* ids, float* lp,
-                          float* lse, const Ws& w, cudaStream_t s) {
-  dflash2_status_t st = run_partials(p, rows, lm_head, w, s);
-  if (st != DFLASH2_OK) return st;
-  return run_merge(p, ids, lp, lse, w, s);
-}
-
 dflash2_status_t run_walk(const Plan& p, const int32_t* anchor, const int32_t* ids, const float* lp,
-                          const void* U, const void* V, int32_t* path_ids, int32_t* path_idx, float* score,
-                          const Ws& w, cudaStream_t s) {
-  return cuda_status(df::launch_transition_walk(p.bf16, anchor, ids, lp, U, V, p.B, p.T, p.K, p.R, p.V,
+                          const void* U, const void* V, const float* gate, int32_t* path_ids, int32_t* path_idx,
+                          float* score, const Ws& w, cudaStream_t s) {
+  return cuda_status(df::launch_transition_walk(p.bf16, anchor, ids, lp, U, V, gate, p.B, p.T, p.K, p.R, p.V,
                                                 p.greedy ? 1 : 0, path_ids, path_idx, score, w.err, s));
 }
 
@@ -368,14 +378,24 @@ dflash2_status_t dflash2_conv(const dflash2_shape_t* shape, const void* x, const
 dflash2_status_t dflash2_select_topk(const dflash2_shape_t* shape, const void* rows, const void* lm_head,
                                      int32_t* cand_ids, float* cand_lp, float* lse, void* ws, size_t ws_bytes,
                                      void* stream) {
+  return dflash2_select_topk_gated(shape, rows, lm_head, nullptr, cand_ids, cand_lp, lse, nullptr, ws, ws_bytes,
+                                   stream);
+}
+
+dflash2_status_t dflash2_select_topk_gated(const dflash2_shape_t* shape, const void* rows, const void* lm_head,
+                                           const void* gate_w, int32_t* cand_ids, float* cand_lp, float* lse,
+                                           float* gate, void* ws, size_t ws_bytes, void* stream) {
   Plan p;
   dflash2_status_t st = make_plan(shape, p);
   if (st != DFLASH2_OK) return st;
-  if (!rows || !lm_head || !cand_ids || !cand_lp) return DFLASH2_ERR_INVALID_ARGUMENT;
-  if (!aligned16(rows) || !aligned16(lm_head)) return DFLASH2_ERR_INVALID_ARGUMENT;
+  if (!rows || !lm_head || !cand_ids || !cand_lp || (gate_w && !gate)) return DFLASH2_ERR_INVALID_ARGUMENT;
+  if (!aligned16(rows) || !aligned16(lm_head) || (gate_w && !aligned16(gate_w))) return DFLASH2_ERR_INVALID_ARGUMENT;
+  if (gate_w && !p.bf16) return DFLASH2_ERR_UNSUPPORTED;
   Ws w;
   if ((st = check_ws(p, ws, ws_bytes, w)) != DFLASH2_OK) return st;
-  return run_topk(p, rows, lm_head, cand_ids, cand_lp, lse, w, static_cast<cudaStream_t>(stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((st = run_partials(p, rows, lm_head, w, s, gate_w, gate)) != DFLASH2_OK) return st;
+  return run_merge(p, cand_ids, cand_lp, lse, w, s);
 }
 
 dflash2_status_t dflash2_select_topk_noalloc(const dflash2_shape_t* shape, const void* rows, const void* lm_head,
@@ -422,15 +442,23 @@ dflash2_status_t dflash2_merge_partials(const dflash2_shape_t* shape, int32_t* c
 dflash2_status_t dflash2_viterbi(const dflash2_shape_t* shape, const int32_t* anchor, const int32_t* cand_ids,
                                  const float* cand_lp, const void* U, const void* V, int32_t* path_ids,
                                  int32_t* path_idx, float* score, void* ws, size_t ws_bytes, void* stream) {
+  return dflash2_viterbi_gated(shape, anchor, cand_ids, cand_lp, U, V, nullptr, path_ids, path_idx, score, ws,
+                               ws_bytes, stream);
+}
+
+dflash2_status_t dflash2_viterbi_gated(const dflash2_shape_t* shape, const int32_t* anchor, const int32_t* cand_ids,
+                                       const float* cand_lp, const void* U, const void* V, const float* gate,
+                                       int32_t* path_ids, int32_t* path_idx, float* score, void* ws,
+                                       size_t ws_bytes, void* stream) {
   Plan p;
   dflash2_status_t st = make_plan(shape, p);
   if (st != DFLASH2_OK) return st;
   if (!anchor || !cand_ids || !cand_lp || !U || !V || !path_ids || !path_idx || !score)
     return DFLASH2_ERR_INVALID_ARGUMENT;
-  if (!aligned16(U) || !aligned16(V)) return DFLASH2_ERR_INVALID_ARGUMENT;
+  if (!aligned16(U) || !aligned16(V) || (gate && !aligned16(gate))) return DFLASH2_ERR_INVALID_ARGUMENT;
   Ws w;
   if ((st = check_ws(p, ws, ws_bytes, w)) != DFLASH2_OK) return st;
-  return run_walk(p, anchor, cand_ids, cand_lp, U, V, path_ids, path_idx, score, w,
+  return run_walk(p, anchor, cand_ids, cand_lp, U, V, gate, path_ids, path_idx, score, w,
                   static_cast<cudaStream_t>(stream));
 }
 
@@ -438,14 +466,25 @@ dflash2_status_t dflash2_draft_tail(const dflash2_shape_t* shape, const void* hi
                                     const void* U, const void* V, const void* conv_w, const int32_t* anchor,
                                     int32_t* path_ids, int32_t* path_idx, float* score, int32_t* cand_ids,
                                     float* cand_lp, float* lse, void* ws, size_t ws_bytes, void* stream) {
+  return dflash2_draft_tail_gated(shape, hidden, lm_head, U, V, conv_w, nullptr, anchor, path_ids, path_idx, score,
+                                  cand_ids, cand_lp, lse, nullptr, ws, ws_bytes, stream);
+}
+
+dflash2_status_t dflash2_draft_tail_gated(const dflash2_shape_t* shape, const void* hidden, const void* lm_head,
+                                          const void* U, const void* V, const void* conv_w, const void* gate_w,
+                                          const int32_t* anchor, int32_t* path_ids, int32_t* path_idx, float* score,
+                                          int32_t* cand_ids, float* cand_lp, float* lse, float* gate,
+                                          void* ws, size_t ws_bytes, void* stream) {
   Plan p;
   dflash2_status_t st = make_plan(shape, p);
   if (st != DFLASH2_OK) return st;
   if (!hidden || !lm_head || !U || !V || (p.NL > 0 && !conv_w) || !anchor || !path_ids || !path_idx || !score)
     return DFLASH2_ERR_INVALID_ARGUMENT;
   if (!aligned16(hidden) || !aligned16(lm_head) || !aligned16(U) || !aligned16(V) ||
-      (conv_w && !aligned16(conv_w)))
+      (conv_w && !aligned16(conv_w)) || (gate_w && !aligned16(gate_w)))
     return DFLASH2_ERR_INVALID_ARGUMENT;
+  if (gate && !aligned16(gate)) return DFLASH2_ERR_INVALID_ARGUMENT;
+  if (gate_w && !p.bf16) return DFLASH2_ERR_UNSUPPORTED;
   Ws w;
   if ((st = check_ws(p, ws, ws_bytes, w)) != DFLASH2_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -458,15 +497,17 @@ dflash2_status_t dflash2_draft_tail(const dflash2_shape_t* shape, const void* hi
     if ((st = run_conv(p, hidden, conv_w, zbuf, w, s)) != DFLASH2_OK) return st;
     z = zbuf;
   }
-  if ((st = run_partials(p, z, lm_head, w, s)) != DFLASH2_OK) return st;
+  // the gate rows: the caller's buffer when given, else the workspace's
+  float* g = gate_w ? (gate ? gate : w.gate) : nullptr;
+  if ((st = run_partials(p, z, lm_head, w, s, gate_w, g)) != DFLASH2_OK) return st;
   if (df::select_walk_smem(p.lm_parts) <= 227 * 1024)  // merge fused with the walk
     return cuda_status(df::launch_select_walk(p.bf16, w.part_val, w.part_id, w.part_ms, p.lm_parts, p.M, anchor, U,
-                                              V, p.B, p.T, p.K, p.R, p.V, p.greedy ? 1 : 0, cand_ids, cand_lp, lse,
-                                              path_ids, path_idx, score, w.err, s));
+                                              V, g, p.B, p.T, p.K, p.R, p.V, p.greedy ? 1 : 0, cand_ids, cand_lp,
+                                              lse, path_ids, path_idx, score, w.err, s));
   int32_t* ids = cand_ids ? cand_ids : w.cand_ids;
   float* lp = cand_lp ? cand_lp : w.cand_lp;
   if ((st = run_merge(p, ids, lp, lse, w, s)) != DFLASH2_OK) return st;
-  return run_walk(p, anchor, ids, lp, U, V, path_ids, path_idx, score, w, s);
+  return run_walk(p, anchor, ids, lp, U, V, g, path_ids, path_idx, score, w, s);
 }
 
 dflash2_status_t dflash2_read_device_error(void* ws, void* stream, int32_t* code_out) {

@@ -10,10 +10,12 @@
 namespace df {
 
 // tcgen05 GEMM + top-K/lse partials (bf16). grid = n_rc * parts.
+// g16: 16-row box map of the gate matrix (any valid map when args.gate_cols == 0); vocab: the
+// ranked columns; gate_out [M, gate_cols] fp32 receives the gate columns.
 cudaError_t launch_lmhead_topk_bf16(const CUtensorMap& a, const CUtensorMap& a_tail, const CUtensorMap& b128,
-                                    const CUtensorMap& b16,
-                                    const TcGemmArgs& args, float* part_val, int32_t* part_id,
-                                    float* part_ms, cudaStream_t s);
+                                    const CUtensorMap& b16, const CUtensorMap& g16, const TcGemmArgs& args,
+                                    int vocab, float* part_val, int32_t* part_id, float* part_ms,
+                                    float* gate_out, cudaStream_t s);
 
 // tcgen05 GEMM + conv-layer epilogue (bf16): y = mix(x) with taps = x * W^T.
 cudaError_t launch_conv_layer_bf16(const CUtensorMap& a, const CUtensorMap& a_tail, const CUtensorMap& b128,
@@ -70,15 +72,17 @@ cudaError_t launch_topk_merge(const float* part_val, const int32_t* part_id, con
 // (the whole-tail call); cand_ids / cand_lp / lse may be null. Needs select_walk_smem(parts)
 // bytes of shared memory (at most 227 KB).
 size_t select_walk_smem(int parts);
+// gate: [B*T, R] fp32 context gate of every slot, or nullptr (no gate).
 cudaError_t launch_select_walk(bool bf16, const float* part_val, const int32_t* part_id, const float* part_ms,
-                               int parts, int M, const int32_t* anchor, const void* U, const void* V, int B, int T,
-                               int K, int R, int vocab, int greedy, int32_t* cand_ids, float* cand_lp, float* lse,
-                               int32_t* path_ids, int32_t* path_idx, float* score, int32_t* err, cudaStream_t s);
+                               int parts, int M, const int32_t* anchor, const void* U, const void* V,
+                               const float* gate, int B, int T, int K, int R, int vocab, int greedy,
+                               int32_t* cand_ids, float* cand_lp, float* lse, int32_t* path_ids, int32_t* path_idx,
+                               float* score, int32_t* err, cudaStream_t s);
 
 // Transition tiles + Viterbi / greedy walk, one CTA per sequence.
 cudaError_t launch_transition_walk(bool bf16, const int32_t* anchor, const int32_t* cand_ids,
-                                   const float* cand_lp, const void* U, const void* V, int B, int T, int K,
-                                   int R, int vocab, int greedy, int32_t* path_ids, int32_t* path_idx,
+                                   const float* cand_lp, const void* U, const void* V, const float* gate, int B,
+                                   int T, int K, int R, int vocab, int greedy, int32_t* path_ids, int32_t* path_idx,
                                    float* score, int32_t* err, cudaStream_t s);
 
 }  // namespace df

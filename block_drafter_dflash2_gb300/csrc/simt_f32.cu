@@ -105,7 +105,7 @@ cudaError_t launch_conv_layer_f32(const float* x, const float* w, float* y, int 
 cudaError_t launch_lmhead_topk_f32(const float* z, const float* w, const TcGemmArgs& args, float* part_val,
                                    int32_t* part_id, float* part_ms, cudaStream_t s) {
   if (args.M > kMaxRows) return cudaErrorInvalidValue;
-  EpiTopK::Params ep{part_val, part_id, part_ms, args.M};
+  EpiTopK::Params ep{part_val, part_id, part_ms, args.M, args.n_total, nullptr, 0, 0};  // no gate columns
   lmhead_topk_f32_kernel<<<args.parts, 128, 0, s>>>(z, w, args, ep);
   return cudaGetLastError();
 }

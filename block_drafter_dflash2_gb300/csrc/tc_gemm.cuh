@@ -19,6 +19,11 @@
 // keep many more loads in flight. The MMA reads 128 A rows regardless; rows past the box hold
 // stale data and only feed TMEM lanes no epilogue thread reads. TMEM holds two fp32
 // accumulators as wide as a tile, so the epilogue of tile t overlaps the MMAs of tile t+1.
+//
+// Gate columns: the LM-head launch can append the rows of a second matrix (the context gate's
+// [R, H] weights) as extra columns past the vocabulary; they are fetched from their own
+// tensor map in 16-row boxes, balanced over the partitions like any other column, and the
+// epilogue stores their fp32 values instead of ranking them.
 #pragma once
 
 #include "ptx.cuh"
@@ -78,7 +83,8 @@ template <class Epi>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_a_tail,
                    const __grid_constant__ CUtensorMap map_b128, const __grid_constant__ CUtensorMap map_b16,
-                   const TcGemmArgs args, const typename Epi::Params ep) {
+                   const __grid_constant__ CUtensorMap map_g16, const TcGemmArgs args,
+                   const typename Epi::Params ep) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(base);
@@ -127,6 +133,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tma_prefetch_desc(tail_chunk ? &map_a_tail : &map_a);
     tma_prefetch_desc(&map_b128);
     tma_prefetch_desc(&map_b16);
+    if (args.gate_cols > 0) tma_prefetch_desc(&map_g16);
   }
   tc_fence_before();
   __syncthreads();
@@ -161,7 +168,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           uint8_t* sb = sa + sg.b_off;
           mbar_arrive_expect_tx(&full[stage], bytes);
           tma_load_2d(sa, ma, &full[stage], kb * kBK, rc * kBM, pol_a);
-          if (CL == 1) {
+          if (args.gate_cols > 0 && n0 + nu * 16 > args.gate_base) {
+            // a tile reaching the gate columns: 16-row boxes, each from its own matrix
+            for (int j = 0; j < nu; ++j) {
+              const int col = n0 + 16 * j;
+              if (col >= args.gate_base)
+                tma_load_2d(sb + j * 16 * kBK * 2, &map_g16, &full[stage], kb * kBK, col - args.gate_base, pol_b);
+              else
+                tma_load_2d(sb + j * 16 * kBK * 2, &map_b16, &full[stage], kb * kBK, col, pol_b);
+            }
+          } else if (CL == 1) {
             if (nu % 8 == 0) {
               for (int j = 0; j < nu / 8; ++j)
                 tma_load_2d(sb + j * 128 * kBK * 2, &map_b128, &full[stage], kb * kBK, n0 + 128 * j, pol_b);
@@ -289,6 +305,9 @@ struct EpiTopK {
     int32_t* part_id;   // [parts][M][16]
     float* part_ms;     // [parts][M][2]  (running max, sum of exp(l - max))
     int M;
+    int vocab;          // columns ranked (the vocabulary; every launcher must set it)
+    float* gate_out;    // [M][gate_cols] fp32: the gate columns' values (gate_cols > 0)
+    int gate_base, gate_cols;
   };
   struct State {
     float m, s;
@@ -318,9 +337,20 @@ struct EpiTopK {
       st.id[0] = id;
     }
   }
-  static DF_DEV void consume(State& st, const Params&, const float (&v)[32], int, bool row_ok, int col0,
+  static DF_DEV void consume(State& st, const Params& p, const float (&v)[32], int row, bool row_ok, int col0,
                              int ncols, int col_end) {
     if (!row_ok) return;
+    if (col0 + 32 > p.vocab) {
+      // past the vocabulary: store the gate columns of this chunk; rank only the vocabulary
+      if (p.gate_cols > 0) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int c = col0 + i - p.gate_base;
+          if (i < ncols && c >= 0 && c < p.gate_cols) p.gate_out[(size_t)row * p.gate_cols + c] = v[i];
+        }
+      }
+      col_end = min(col_end, p.vocab);
+    }
     const int nvalid = min(ncols, col_end - col0);
     float cm = -INFINITY;
 #pragma unroll

@@ -16,6 +16,11 @@ struct TcGemmArgs {
   int cluster;      // 1; or n_rc (2, 4, 8): the row-chunk CTAs of a column range multicast its
                     // weight tiles to each other (supported, not chosen by the planner: slower)
   int32_t* err;  // device error word
+  // Extra columns from a second matrix (the context gate): columns [gate_base, gate_base +
+  // gate_cols) are rows 0.. of the map_g16 matrix, columns below gate_base rows of map_b.
+  // gate_base is a multiple of 16; gate_cols = 0: every column is from map_b.
+  int gate_base = 0;
+  int gate_cols = 0;
 };
 
 }  // namespace df

@@ -11,6 +11,11 @@
 // lp_t(j), and keeps the back-pointer; a shuffle arg-max (lowest index on ties) picks the
 // final state and lane 0 reads the path back.
 //
+// Context gate (optional): tau_t(i, j) = sum_r U[prev_i][r] g_t[r] V[cur_j][r] with g_t the gate
+// of slot t (fp32, [B*T, R]). The warp that builds tile t scales its staged V rows by g_t and
+// rounds them to bf16 before the MMA (one rounding of V[cur_j][r] g_t[r]; fp32 embeddings keep
+// the product in fp32).
+//
 // The fused kernel first merges the sequence's T rows (warp t % 8 takes row t): the row's
 // per-partition top-16 lists and (max, sum) pairs are staged with cp.async, lse is reduced
 // across the warp and the K best candidates are picked by the warp-wide merge; they stay in
@@ -95,6 +100,28 @@ __device__ __forceinline__ void store_tau(const float (&acc)[2][4], float (&tau)
   }
 }
 
+// Multiplies the 16 staged rows (cols columns each, from column c0 of the embedding) by the
+// gate g[c0 ..], rounding to bf16; one warp, after the rows have landed.
+__device__ __forceinline__ void gate_rows(__nv_bfloat16* st, int cols, const float* __restrict__ g) {
+  const int lane = threadIdx.x & 31;
+  const int vec_per_row = cols / 8;
+  for (int v = lane; v < kKP * vec_per_row; v += 32) {
+    const int row = v / vec_per_row, cv = v % vec_per_row;
+    uint4* p = reinterpret_cast<uint4*>(st + row * kRowPad + cv * 8);
+    const float4 g0 = __ldg(reinterpret_cast<const float4*>(g + cv * 8));
+    const float4 g1 = __ldg(reinterpret_cast<const float4*>(g + cv * 8 + 4));
+    uint4 x = *p;
+    __nv_bfloat162* x2 = reinterpret_cast<__nv_bfloat162*>(&x);
+    const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = __bfloat1622float2(x2[k]);
+      x2[k] = __floats2bfloat162_rn(f.x * gg[2 * k], f.y * gg[2 * k + 1]);
+    }
+    *p = x;
+  }
+}
+
 // Issues (without waiting) the 16-byte copies of rows ids[0..15] of E (R <= kRChunk columns)
 // into the 16 padded rows at st.
 __device__ __forceinline__ void gather_rows(const __nv_bfloat16* __restrict__ E, int R, const int32_t* ids,
@@ -109,8 +136,8 @@ __device__ __forceinline__ void gather_rows(const __nv_bfloat16* __restrict__ E,
 
 // tau tile for one boundary, bf16 embeddings, on one warp.
 __device__ void tile_bf16(const __nv_bfloat16* __restrict__ U, const __nv_bfloat16* __restrict__ V, int R,
-                          const int32_t* prev, const int32_t* cur, __nv_bfloat16* stA, __nv_bfloat16* stB,
-                          float (&tau)[kKP][kKP]) {
+                          const int32_t* prev, const int32_t* cur, const float* g, __nv_bfloat16* stA,
+                          __nv_bfloat16* stB, float (&tau)[kKP][kKP]) {
   const int lane = threadIdx.x & 31;
   float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
   for (int r0 = 0; r0 < R; r0 += kRChunk) {
@@ -126,6 +153,10 @@ __device__ void tile_bf16(const __nv_bfloat16* __restrict__ U, const __nv_bfloat
     cp_async_commit();
     cp_async_wait_all();
     __syncwarp();
+    if (g) {
+      gate_rows(stB, rc, g + r0);
+      __syncwarp();
+    }
     tile_mma(stA, stB, rc, acc);
   }
   store_tau(acc, tau);
@@ -133,14 +164,17 @@ __device__ void tile_bf16(const __nv_bfloat16* __restrict__ U, const __nv_bfloat
 
 // tau tile for one boundary, fp32 embeddings (small instantiation): 8 entries per lane.
 __device__ void tile_f32(const float* __restrict__ U, const float* __restrict__ V, int R, const int32_t* prev,
-                         const int32_t* cur, float (&tau)[kKP][kKP]) {
+                         const int32_t* cur, const float* g, float (&tau)[kKP][kKP]) {
   const int lane = threadIdx.x & 31;
   for (int e = lane; e < kKP * kKP; e += 32) {
     const int i = e / kKP, j = e % kKP;
     const float* u = U + (size_t)prev[i] * R;
     const float* v = V + (size_t)cur[j] * R;
     float s = 0.f;
-    for (int r = 0; r < R; ++r) s = fmaf(u[r], v[r], s);
+    if (g)
+      for (int r = 0; r < R; ++r) s = fmaf(u[r], v[r] * g[r], s);
+    else
+      for (int r = 0; r < R; ++r) s = fmaf(u[r], v[r], s);
     tau[i][j] = s;
   }
 }
@@ -158,8 +192,10 @@ __device__ void pad_candidates(SmemWalk& sw, int T, int K) {
 }
 
 // All T transition tiles of one sequence; warp w builds the tiles t = w, w + 8, ...
+// gate_b: the sequence's gate rows [T, R] (nullptr: no gate).
 template <bool kBf16>
-__device__ void build_tiles(SmemWalk& sw, int T, int R, const void* Uv, const void* Vv, __nv_bfloat16* stage) {
+__device__ void build_tiles(SmemWalk& sw, int T, int R, const void* Uv, const void* Vv, const float* gate_b,
+                            __nv_bfloat16* stage) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   __shared__ int32_t prev_s[kWarps][kKP];
   for (int t = warp; t < T; t += kWarps) {
@@ -171,10 +207,10 @@ __device__ void build_tiles(SmemWalk& sw, int T, int R, const void* Uv, const vo
       __nv_bfloat16* stA = stage + (size_t)warp * 2 * kKP * kRowPad;
       __nv_bfloat16* stB = stA + kKP * kRowPad;
       tile_bf16(reinterpret_cast<const __nv_bfloat16*>(Uv), reinterpret_cast<const __nv_bfloat16*>(Vv), R,
-                prev_s[warp], cur, stA, stB, sw.tau[t]);
+                prev_s[warp], cur, gate_b ? gate_b + (size_t)t * R : nullptr, stA, stB, sw.tau[t]);
     } else {
       tile_f32(reinterpret_cast<const float*>(Uv), reinterpret_cast<const float*>(Vv), R, prev_s[warp], cur,
-               sw.tau[t]);
+               gate_b ? gate_b + (size_t)t * R : nullptr, sw.tau[t]);
     }
     __syncwarp();
   }
@@ -262,9 +298,9 @@ template <bool kBf16>
 __global__ void __launch_bounds__(32 * kWarps)
     transition_walk_kernel(const int32_t* __restrict__ anchor, const int32_t* __restrict__ cand_ids,
                            const float* __restrict__ cand_lp, const void* __restrict__ Uv,
-                           const void* __restrict__ Vv, int T, int K, int R, int vocab, int greedy,
-                           int32_t* __restrict__ path_ids, int32_t* __restrict__ path_idx, float* __restrict__ score,
-                           int32_t* err) {
+                           const void* __restrict__ Vv, const float* __restrict__ gate, int T, int K, int R,
+                           int vocab, int greedy, int32_t* __restrict__ path_ids, int32_t* __restrict__ path_idx,
+                           float* __restrict__ score, int32_t* err) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   SmemWalk& sw = *reinterpret_cast<SmemWalk*>(smem_raw);
   __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(smem_raw + ((sizeof(SmemWalk) + 127) & ~size_t(127)));
@@ -282,7 +318,7 @@ __global__ void __launch_bounds__(32 * kWarps)
   __syncthreads();
   pad_candidates(sw, T, K);
   __syncthreads();
-  build_tiles<kBf16>(sw, T, R, Uv, Vv, stage);
+  build_tiles<kBf16>(sw, T, R, Uv, Vv, gate ? gate + (size_t)b * T * R : nullptr, stage);
   __syncthreads();
   if ((threadIdx.x >> 5) != 0) return;
   walk_warp0(sw, b, T, K, greedy, path_ids, path_idx, score);
@@ -306,7 +342,8 @@ template <bool kBf16>
 __global__ void __launch_bounds__(32 * kWarps)
     select_walk_kernel(const float* __restrict__ part_val, const int32_t* __restrict__ part_id,
                        const float2* __restrict__ part_ms, int parts, int M, const int32_t* __restrict__ anchor,
-                       const void* __restrict__ Uv, const void* __restrict__ Vv, int T, int K, int R, int vocab,
+                       const void* __restrict__ Uv, const void* __restrict__ Vv, const float* __restrict__ gate,
+                       int T, int K, int R, int vocab,
                        int greedy, int32_t* __restrict__ cand_ids, float* __restrict__ cand_lp,
                        float* __restrict__ lse_out, int32_t* __restrict__ path_ids, int32_t* __restrict__ path_idx,
                        float* __restrict__ score, int32_t* err) {
@@ -374,6 +411,9 @@ __global__ void __launch_bounds__(32 * kWarps)
       if (lane == 0 && lse_out) lse_out[row] = lse;
       warp_merge_lists(sv, si, head, parts, K, [&](int k, int32_t id, float v) {
         const float lp = v - lse;
+        // every merged id indexes U and V below: a partial that held no column would carry an
+        // out-of-range id, so clamp (and flag) as for the caller's candidates
+        id = clamp_id(id, vocab, err, DFLASH2_DEVERR_CANDIDATE_RANGE);
         sw.ids[t][k] = id;
         sw.lp[t][k] = lp;
         if (cand_ids) cand_ids[(size_t)row * K + k] = id;
@@ -401,7 +441,11 @@ __global__ void __launch_bounds__(32 * kWarps)
     if (warp < T) {
       const __nv_bfloat16* stA =
           warp == 0 ? a0 : reinterpret_cast<const __nv_bfloat16*>(region + (warp - 1) * wstride) + kKP * kRowPad;
-      const __nv_bfloat16* stB = reinterpret_cast<const __nv_bfloat16*>(region + warp * wstride);
+      __nv_bfloat16* stB = reinterpret_cast<__nv_bfloat16*>(region + warp * wstride);
+      if (gate) {
+        gate_rows(stB, R, gate + ((size_t)b * T + warp) * R);
+        __syncwarp();
+      }
       float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
       tile_mma(stA, stB, R, acc);
       store_tau(acc, sw.tau[warp]);
@@ -411,7 +455,8 @@ __global__ void __launch_bounds__(32 * kWarps)
     __syncthreads();
     pad_candidates(sw, T, K);
     __syncthreads();
-    build_tiles<kBf16>(sw, T, R, Uv, Vv, reinterpret_cast<__nv_bfloat16*>(region));
+    build_tiles<kBf16>(sw, T, R, Uv, Vv, gate ? gate + (size_t)b * T * R : nullptr,
+                       reinterpret_cast<__nv_bfloat16*>(region));
     __syncthreads();
   }
   if (warp != 0) return;
@@ -428,9 +473,10 @@ size_t select_walk_smem(int parts) {
 }
 
 cudaError_t launch_select_walk(bool bf16, const float* part_val, const int32_t* part_id, const float* part_ms,
-                               int parts, int M, const int32_t* anchor, const void* U, const void* V, int B, int T,
-                               int K, int R, int vocab, int greedy, int32_t* cand_ids, float* cand_lp, float* lse,
-                               int32_t* path_ids, int32_t* path_idx, float* score, int32_t* err, cudaStream_t s) {
+                               int parts, int M, const int32_t* anchor, const void* U, const void* V,
+                               const float* gate, int B, int T, int K, int R, int vocab, int greedy,
+                               int32_t* cand_ids, float* cand_lp, float* lse, int32_t* path_ids, int32_t* path_idx,
+                               float* score, int32_t* err, cudaStream_t s) {
   if (T > kMaxT || K > kKP) return cudaErrorInvalidValue;
   const size_t smem = select_walk_smem(parts);
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
@@ -451,23 +497,23 @@ cudaError_t launch_select_walk(bool bf16, const float* part_val, const int32_t* 
     static unsigned char smem_done[64];
     e = smem_opt_in(reinterpret_cast<const void*>(select_walk_kernel<true>), smem_done);
     if (e != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, select_walk_kernel<true>, part_val, part_id, ms, parts, M, anchor, U, V, T, K, R,
-                           vocab, greedy, cand_ids, cand_lp, lse, path_ids, path_idx, score, err);
+    e = cudaLaunchKernelEx(&cfg, select_walk_kernel<true>, part_val, part_id, ms, parts, M, anchor, U, V, gate, T, K,
+                           R, vocab, greedy, cand_ids, cand_lp, lse, path_ids, path_idx, score, err);
     if (e != cudaSuccess) return e;
   } else {
     static unsigned char smem_done[64];
     e = smem_opt_in(reinterpret_cast<const void*>(select_walk_kernel<false>), smem_done);
     if (e != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, select_walk_kernel<false>, part_val, part_id, ms, parts, M, anchor, U, V, T, K,
-                           R, vocab, greedy, cand_ids, cand_lp, lse, path_ids, path_idx, score, err);
+    e = cudaLaunchKernelEx(&cfg, select_walk_kernel<false>, part_val, part_id, ms, parts, M, anchor, U, V, gate, T,
+                           K, R, vocab, greedy, cand_ids, cand_lp, lse, path_ids, path_idx, score, err);
     if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }
 
 cudaError_t launch_transition_walk(bool bf16, const int32_t* anchor, const int32_t* cand_ids,
-                                   const float* cand_lp, const void* U, const void* V, int B, int T, int K,
-                                   int R, int vocab, int greedy, int32_t* path_ids, int32_t* path_idx,
+                                   const float* cand_lp, const void* U, const void* V, const float* gate, int B,
+                                   int T, int K, int R, int vocab, int greedy, int32_t* path_ids, int32_t* path_idx,
                                    float* score, int32_t* err, cudaStream_t s) {
   if (T > kMaxT || K > kKP) return cudaErrorInvalidValue;
   const size_t base = (sizeof(SmemWalk) + 127) & ~size_t(127);
@@ -477,14 +523,14 @@ cudaError_t launch_transition_walk(bool bf16, const int32_t* anchor, const int32
     static unsigned char smem_done[64];
     e = smem_opt_in(reinterpret_cast<const void*>(transition_walk_kernel<true>), smem_done);
     if (e != cudaSuccess) return e;
-    transition_walk_kernel<true><<<B, 32 * kWarps, smem, s>>>(anchor, cand_ids, cand_lp, U, V, T, K, R, vocab,
-                                                               greedy, path_ids, path_idx, score, err);
+    transition_walk_kernel<true><<<B, 32 * kWarps, smem, s>>>(anchor, cand_ids, cand_lp, U, V, gate, T, K, R,
+                                                               vocab, greedy, path_ids, path_idx, score, err);
   } else {
     static unsigned char smem_done[64];
     e = smem_opt_in(reinterpret_cast<const void*>(transition_walk_kernel<false>), smem_done);
     if (e != cudaSuccess) return e;
-    transition_walk_kernel<false><<<B, 32 * kWarps, smem, s>>>(anchor, cand_ids, cand_lp, U, V, T, K, R, vocab,
-                                                                greedy, path_ids, path_idx, score, err);
+    transition_walk_kernel<false><<<B, 32 * kWarps, smem, s>>>(anchor, cand_ids, cand_lp, U, V, gate, T, K, R,
+                                                                vocab, greedy, path_ids, path_idx, score, err);
   }
   return cudaGetLastError();
 }

@@ -116,6 +116,24 @@ dflash2_status_t dflash2_select_topk(const dflash2_shape_t* shape, const void* r
                                      int32_t* cand_ids, float* cand_lp, float* lse,
                                      void* ws, size_t ws_bytes, void* stream);
 
+/* Context gate (optional; "DFlash 2: keeping drafts parallel", section "軽量パスセレクター"
+ * (lightweight path selector): S_t(a, b) = U_t(b) + <A(a) (.) H(h_t), B(b)>, where the context
+ * gate H(h_t) decides which part of the embedding match counts). The pages give no formula for
+ * H; here it is a linear map of the slot's hidden row h_t (the row the LM head reads):
+ *   gate[m, r] = sum_h rows[m, h] * gate_w[r, h],   gate_w [R, H] (bf16), gate [M, R] fp32,
+ * and the gated transition is tau_t(i, j) = sum_r U[prev_i, r] * gate[slot t, r] * V[cur_j, r]
+ * (the gate of the current slot t; for t = 0 the anchor is the previous token).
+ * The gate is contracted in the LM-head pass itself (its R rows are appended to the head's
+ * columns), so it costs no extra pass over the rows. bf16 only; dtype FP32 returns
+ * DFLASH2_ERR_UNSUPPORTED. In the walk, V[cur_j, r] * gate[r] is rounded to bf16 once before
+ * the fp32-accumulated product with U (fp32 embeddings keep it in fp32).
+ *
+ * dflash2_select_topk_gated: dflash2_select_topk plus gate [M, R] fp32 out (gate_w non-NULL;
+ * gate_w NULL is dflash2_select_topk, gate ignored). */
+dflash2_status_t dflash2_select_topk_gated(const dflash2_shape_t* shape, const void* rows, const void* lm_head,
+                                           const void* gate_w, int32_t* cand_ids, float* cand_lp, float* lse,
+                                           float* gate, void* ws, size_t ws_bytes, void* stream);
+
 /* dflash2_select_topk without a workspace argument and without any allocation, for callers
  * that cannot obtain device memory at the point of the call: a plugin inside a serving
  * engine that has already reserved the whole GPU for its own pools and exposes no
@@ -168,6 +186,14 @@ dflash2_status_t dflash2_viterbi(const dflash2_shape_t* shape, const int32_t* an
                                  int32_t* path_ids, int32_t* path_idx, float* score,
                                  void* ws, size_t ws_bytes, void* stream);
 
+/* dflash2_viterbi with the context gate: gate [B, T, R] fp32 (16-byte aligned) is each slot's
+ * gate row as above; NULL is dflash2_viterbi. */
+dflash2_status_t dflash2_viterbi_gated(const dflash2_shape_t* shape, const int32_t* anchor,
+                                       const int32_t* cand_ids, const float* cand_lp,
+                                       const void* U, const void* V, const float* gate,
+                                       int32_t* path_ids, int32_t* path_idx, float* score,
+                                       void* ws, size_t ws_bytes, void* stream);
+
 /* The whole tail in one call: conv -> LM head top-K + lse -> transitions + walk.
  *   hidden [B, T, H], lm_head [V, H], U/V [V, R], conv_w [NL, 2H/16, H], anchor [B]
  *   path_ids, path_idx [B, T] int32; score [B] fp32
@@ -178,6 +204,15 @@ dflash2_status_t dflash2_draft_tail(const dflash2_shape_t* shape, const void* hi
                                     const int32_t* anchor, int32_t* path_ids, int32_t* path_idx,
                                     float* score, int32_t* cand_ids, float* cand_lp, float* lse,
                                     void* ws, size_t ws_bytes, void* stream);
+
+/* dflash2_draft_tail with the context gate: gate_w [R, H] (bf16) as above; the gate rows are
+ * formed in the LM-head pass from the conv output and applied in the walk. gate [B, T, R] fp32
+ * receives them (NULL: kept in the workspace only). gate_w NULL is dflash2_draft_tail. */
+dflash2_status_t dflash2_draft_tail_gated(const dflash2_shape_t* shape, const void* hidden, const void* lm_head,
+                                          const void* U, const void* V, const void* conv_w, const void* gate_w,
+                                          const int32_t* anchor, int32_t* path_ids, int32_t* path_idx,
+                                          float* score, int32_t* cand_ids, float* cand_lp, float* lse,
+                                          float* gate, void* ws, size_t ws_bytes, void* stream);
 
 /* Synchronises `stream`, returns the workspace's device error word in *code_out
  * (a DFLASH2_DEVERR_* bit set; 0 = none) and clears it. Returns DFLASH2_OK, or

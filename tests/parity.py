@@ -10,6 +10,10 @@ oracle's conv; the LM-head selection against the oracle run on the GPU's own z (
 of difference in z moves a logit by ~1e-3, more than the near-tie band); the walk exactly on
 the GPU's own candidates. Agreement with the oracle end to end is reported as well.
 
+With the context gate, the gate rows are compared with the oracle's H(h_t) of the GPU's own
+conv output within 1e-3 absolute (they are O(1)), and the walk is checked on the GPU's own
+candidates and gate rows.
+
 Near-tie rules used here:
   * top-K: the GPU's k-th candidate may differ from the oracle's k-th only if the two
     tokens' oracle logits lie within 1e-3 * |max logit| of each other (at the K/K+1
@@ -33,6 +37,7 @@ SCORE_TOL = 2e-3
 CONV_RTOL = 1e-2
 TIE_REL = 1e-3
 MARGIN = 1e-2
+GATE_TOL = 1e-3
 
 
 def shape_of(sh, greedy=False) -> df2.Shape:
@@ -61,10 +66,12 @@ def workspace(shape: df2.Shape) -> torch.Tensor:
 
 
 def upload_inputs(inp: dict) -> dict:
-    return {k: dev(v) for k, v in inp.items() if v is not None and k in ("hidden", "lm_head", "U", "V", "conv_w", "anchor")}
+    return {k: dev(v) for k, v in inp.items()
+            if v is not None and k in ("hidden", "lm_head", "U", "V", "conv_w", "anchor", "gate_w")}
 
 
-def run_tail(shape: df2.Shape, d: dict, ws=None, stream=None) -> dict:
+def run_tail(shape: df2.Shape, d: dict, ws=None, stream=None, gated=False) -> dict:
+    """The whole tail through dflash2_draft_tail, or dflash2_draft_tail_gated (gate rows out)."""
     B, T, K = shape.batch, shape.block, shape.top_k
     o = {
         "path_ids": torch.empty((B, T), dtype=torch.int32, device="cuda:0"),
@@ -75,9 +82,15 @@ def run_tail(shape: df2.Shape, d: dict, ws=None, stream=None) -> dict:
         "lse": torch.empty((B, T), dtype=torch.float32, device="cuda:0"),
     }
     ws = workspace(shape) if ws is None else ws
-    df2.draft_tail(shape, d["hidden"], d["lm_head"], d["U"], d["V"], d["conv_w"], d["anchor"], o["path_ids"],
-                   o["path_idx"], o["score"], ws, cand_ids=o["cand_ids"], cand_lp=o["cand_lp"], lse=o["lse"],
-                   stream=stream)
+    if gated:
+        o["gate"] = torch.empty((B, T, shape.rank), dtype=torch.float32, device="cuda:0")
+        df2.draft_tail_gated(shape, d["hidden"], d["lm_head"], d["U"], d["V"], d["conv_w"], d["gate_w"], d["anchor"],
+                             o["path_ids"], o["path_idx"], o["score"], ws, cand_ids=o["cand_ids"],
+                             cand_lp=o["cand_lp"], lse=o["lse"], gate=o["gate"], stream=stream)
+    else:
+        df2.draft_tail(shape, d["hidden"], d["lm_head"], d["U"], d["V"], d["conv_w"], d["anchor"], o["path_ids"],
+                       o["path_idx"], o["score"], ws, cand_ids=o["cand_ids"], cand_lp=o["cand_lp"], lse=o["lse"],
+                       stream=stream)
     torch.cuda.synchronize()
     err = df2.read_device_error(ws)
     out = {k: host(v) for k, v in o.items()}
@@ -111,13 +124,17 @@ def run_topk(shape: df2.Shape, rows: torch.Tensor, lm_head: torch.Tensor):
     return host(ids), host(lp), host(lse)
 
 
-def run_viterbi(shape: df2.Shape, anchor, cand_ids, cand_lp, U, V):
+def run_viterbi(shape: df2.Shape, anchor, cand_ids, cand_lp, U, V, gate=None):
+    """dflash2_viterbi, or dflash2_viterbi_gated when gate [B,T,R] fp32 is given."""
     B, T = shape.batch, shape.block
     pid = torch.empty((B, T), dtype=torch.int32, device="cuda:0")
     pix = torch.empty((B, T), dtype=torch.int32, device="cuda:0")
     sc = torch.empty((B,), dtype=torch.float32, device="cuda:0")
     ws = workspace(shape)
-    df2.viterbi(shape, anchor, cand_ids, cand_lp, U, V, pid, pix, sc, ws)
+    if gate is None:
+        df2.viterbi(shape, anchor, cand_ids, cand_lp, U, V, pid, pix, sc, ws)
+    else:
+        df2.viterbi_gated(shape, anchor, cand_ids, cand_lp, U, V, gate, pid, pix, sc, ws)
     torch.cuda.synchronize()
     err = df2.read_device_error(ws)
     return host(pid), host(pix), host(sc), err
@@ -178,12 +195,13 @@ def check_topk(ref: dict, g_ids, g_lp, g_lse, z_rows, lm_head, K):
 
 
 def check_walk(shape, anchor, U, V, g_ids, g_lp, g_path_idx, g_path_ids, g_score, ref=None, tie_rows=(),
-               greedy=False):
-    """Exact check of the walk on the GPU's own candidates, and (when given) against the full oracle."""
+               greedy=False, gate=None):
+    """Exact check of the walk on the GPU's own candidates (and gate rows [B,T,R], when gated),
+    and (when given) against the full oracle."""
     B, T, K = shape.batch, shape.block, shape.top_k
     g_ids = g_ids.reshape(B, T, K)
     g_lp = g_lp.reshape(B, T, K)
-    tau = O.transitions(anchor, g_ids, U, V)
+    tau = O.transitions(anchor, g_ids, U, V, gate)
     if greedy:
         o_path, o_score = O.greedy_walk(g_lp, tau)
         best = second = None
@@ -215,6 +233,14 @@ def check_walk(shape, anchor, U, V, g_ids, g_lp, g_path_idx, g_path_ids, g_score
     return stats
 
 
+def check_gate(g_gpu: np.ndarray, g_ref: np.ndarray) -> dict:
+    """Gate rows within GATE_TOL absolute (they are O(1) sums of H bf16 products; fp32 sums in
+    the MMA order against the oracle's float64 sums rounded once)."""
+    err = np.abs(g_gpu.astype(np.float64) - g_ref.astype(np.float64))
+    assert err.max() <= GATE_TOL, f"gate: max abs error {err.max():.3e} > {GATE_TOL}"
+    return {"gate_max_abs_err": float(err.max())}
+
+
 def check_tail(shape, inp: dict, ref: dict, g: dict, seqs=None) -> dict:
     """Compare a draft_tail result with the oracle on the listed sequences, step by step (see
     the module docstring); ref is the oracle's end-to-end result for those sequences."""
@@ -232,13 +258,19 @@ def check_tail(shape, inp: dict, ref: dict, g: dict, seqs=None) -> dict:
     g_lp = g["cand_lp"].reshape(B * T, K)[rows]
     g_lse = g["lse"].reshape(B * T)[rows]
     rep.update(check_topk(ref_g, g_ids, g_lp, g_lse, z_rows, inp["lm_head"], K))
+    g_gate = None
+    if getattr(shape, "gate", False):
+        # the gate rows: H(h_t) of the GPU's own conv output (fp32 sums of bf16 products)
+        g_gate = g["gate"][sel]
+        rep.update(check_gate(g_gate.reshape(-1, g_gate.shape[-1]), ref_g["gate"].reshape(-1, g_gate.shape[-1])))
 
     class _S:  # the subset as a shape
         batch, block, top_k = len(seqs), T, K
     # 3. walk: exact on the GPU's candidates, and against the oracle's path from the same z
     rep.update(check_walk(_S, np.asarray(inp["anchor"])[sel], inp["U"], inp["V"], g_ids, g_lp,
                           g["path_idx"][sel], g["path_ids"][sel], g["score"][sel], ref=ref_g,
-                          tie_rows=rep["near_tie_rows"], greedy=bool(getattr(shape, "greedy", False))))
+                          tie_rows=rep["near_tie_rows"], greedy=bool(getattr(shape, "greedy", False)),
+                          gate=g_gate))
     # end to end against the oracle's own conv: reported, not asserted
     e2e_ids = ref["cand_ids"].reshape(-1, K)
     rep["e2e_rows_same_ids"] = float(np.mean([np.array_equal(a, b) for a, b in zip(g_ids, e2e_ids)]))
