@@ -369,6 +369,28 @@ def run_ours(args, rank, world, local_rank):
                 "lmhead_hbm_gbs": round(lmhead_alg_bytes(sh, b2 * T) / (lmu * 1e-6) / 1e9, 1),
                 "lmhead_tflops": round(2.0 * b2 * T * H * sh.vocab / (lmu * 1e-6) / 1e12, 1)}
 
+    if not args.no_extra and world == 1:
+        # the same workload with the context gate H(h_t): gate rows contracted in the LM-head
+        # pass (R extra columns), applied to the transitions in the walk
+        gw = up(inp["gate_w"])
+        gate_o = torch.empty((B, T, sh.rank), dtype=torch.float32, device=dev)
+
+        def call_g():
+            df2.draft_tail_gated(shape, d["hidden"], d["lm_head"], d["U"], d["V"], d["conv_w"], gw, d["anchor"],
+                                 out["pid"], out["pix"], out["score"], ws, gate=gate_o, stream=stream)
+        with torch.cuda.stream(stream):
+            call_g()
+        torch.cuda.synchronize(dev)
+        assert df2.read_device_error(ws, stream) == 0
+        gg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gg, stream=stream):
+            call_g()
+        msg = timed(gg.replay, args.steps, 3)
+        usg = statistics.mean(msg) * 1e3
+        extra["B=1 gated"] = {"us_per_call": round(usg, 2), "blocks_per_s": round(B / (usg * 1e-6), 1),
+                              "tail_roofline_frac": round(tail_roofline_us(sh, M, bw, tf) / usg, 4),
+                              "over_ungated_us": round(usg - total_ms / args.steps * 1e3, 2)}
+
     us = total_ms / args.steps * 1e3
     lm_us = statistics.mean(lm_ms) * 1e3
     achieved = lmhead_alg_bytes(sh, M) / (lm_us * 1e-6) / 1e9

@@ -167,6 +167,10 @@ dflash2_status_t make_plan(const dflash2_shape_t* s, Plan& p) {
 
 size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Partitions of a gated LM-head pass: the vocabulary's, less one, plus the gate's own (at least
+// one of each). The workspace holds partials for this many.
+int gated_parts(const Plan& p) { return p.lm_parts >= 2 ? p.lm_parts : 2; }
+
 struct Ws {
   int32_t* err;
   unsigned* bar;
@@ -197,9 +201,10 @@ Ws carve(const Plan& p, void* base) {
   w.conv0 = take(act);
   w.conv1 = take(act);
   w.conv_part = static_cast<float*>(take(p.split ? p.split_plan.part_bytes : 0));
-  w.part_val = static_cast<float*>(take((size_t)p.lm_parts * p.M * 16 * 4));
-  w.part_id = static_cast<int32_t*>(take((size_t)p.lm_parts * p.M * 16 * 4));
-  w.part_ms = static_cast<float*>(take((size_t)p.lm_parts * p.M * 2 * 4));
+  const size_t np = (size_t)gated_parts(p);
+  w.part_val = static_cast<float*>(take(np * p.M * 16 * 4));
+  w.part_id = static_cast<int32_t*>(take(np * p.M * 16 * 4));
+  w.part_ms = static_cast<float*>(take(np * p.M * 2 * 4));
   w.cand_ids = static_cast<int32_t*>(take((size_t)p.M * p.K * 4));
   w.cand_lp = static_cast<float*>(take((size_t)p.M * p.K * 4));
   w.gate = static_cast<float*>(take((size_t)p.M * p.R * 4));
@@ -270,22 +275,29 @@ dflash2_status_t run_partials(const Plan& p, const void* rows, const void* lm_he
   TcGemmArgs a{p.M, p.H, p.V, p.n_rc, p.lm_parts, p.a_tail_rows, (p.n_rc > 1 || p.M >= 32) ? 16 : 8,
                p.lm_cluster, w.err};
   if (gate_w) {
+    // the gate rows are one more partition: the last CTA's (the vocabulary keeps the others)
     if (!p.bf16 || !gate_out) return DFLASH2_ERR_UNSUPPORTED;
+    a.parts = gated_parts(p);
     a.gate_base = (p.V + 15) / 16 * 16;
     a.gate_cols = p.R;
-    a.n_total = a.gate_base + p.R;
   }
   if (p.bf16) {
-    CUtensorMap ma, mat, mb128, mb16, mg16;
+    CUtensorMap ma, mat, mb128, mb16, mg128, mg16;
     if (!encode_bf16_2d(&ma, rows, p.H, p.M, 128) || !encode_bf16_2d(&mat, rows, p.H, p.M, p.a_tail_rows) ||
         !encode_bf16_2d(&mb128, lm_head, p.H, p.V, 128) || !encode_bf16_2d(&mb16, lm_head, p.H, p.V, 16))
       return DFLASH2_ERR_CUDA;
     if (gate_w) {
       if (!encode_bf16_2d(&mg16, gate_w, p.H, p.R, 16)) return DFLASH2_ERR_CUDA;
+      if (p.R >= 128) {
+        if (!encode_bf16_2d(&mg128, gate_w, p.H, p.R, 128)) return DFLASH2_ERR_CUDA;
+      } else {
+        mg128 = mg16;  // unused below 128 gate rows
+      }
     } else {
+      mg128 = mb128;
       mg16 = mb16;
     }
-    if (df::launch_lmhead_topk_bf16(ma, mat, mb128, mb16, mg16, a, p.V, w.part_val, w.part_id, w.part_ms,
+    if (df::launch_lmhead_topk_bf16(ma, mat, mb128, mb16, mg128, mg16, a, p.V, w.part_val, w.part_id, w.part_ms,
                                     gate_w ? gate_out : nullptr, s) != cudaSuccess)
       return DFLASH2_ERR_CUDA;
   } else {
@@ -296,9 +308,11 @@ dflash2_status_t run_partials(const Plan& p, const void* rows, const void* lm_he
   return DFLASH2_OK;
 }
 
-dflash2_status_t run_merge(const Plan& p, int32_t* ids, float* lp, float* lse, const Ws& w, cudaStream_t s) {
-  return cuda_status(
-      df::launch_topk_merge(w.part_val, w.part_id, w.part_ms, p.lm_parts, p.M, p.K, ids, lp, lse ? lse : w.lse, s));
+// parts: the partitions the LM-head pass wrote (gated_parts(p) after a gated pass)
+dflash2_status_t run_merge(const Plan& p, int32_t* ids, float* lp, float* lse, const Ws& w, cudaStream_t s,
+                           int parts = 0) {
+  return cuda_status(df::launch_topk_merge(w.part_val, w.part_id, w.part_ms, parts > 0 ? parts : p.lm_parts, p.M,
+                                           p.K, ids, lp, lse ? lse : w.lse, s));
 }
 
 dflash2_status_t run_walk(const Plan& p, const int32_t* anchor, const int32_t* ids, const float* lp,
@@ -395,7 +409,7 @@ dflash2_status_t dflash2_select_topk_gated(const dflash2_shape_t* shape, const v
   if ((st = check_ws(p, ws, ws_bytes, w)) != DFLASH2_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if ((st = run_partials(p, rows, lm_head, w, s, gate_w, gate)) != DFLASH2_OK) return st;
-  return run_merge(p, cand_ids, cand_lp, lse, w, s);
+  return run_merge(p, cand_ids, cand_lp, lse, w, s, gate_w ? gated_parts(p) : p.lm_parts);
 }
 
 dflash2_status_t dflash2_select_topk_noalloc(const dflash2_shape_t* shape, const void* rows, const void* lm_head,
@@ -500,13 +514,14 @@ dflash2_status_t dflash2_draft_tail_gated(const dflash2_shape_t* shape, const vo
   // the gate rows: the caller's buffer when given, else the workspace's
   float* g = gate_w ? (gate ? gate : w.gate) : nullptr;
   if ((st = run_partials(p, z, lm_head, w, s, gate_w, g)) != DFLASH2_OK) return st;
-  if (df::select_walk_smem(p.lm_parts) <= 227 * 1024)  // merge fused with the walk
-    return cuda_status(df::launch_select_walk(p.bf16, w.part_val, w.part_id, w.part_ms, p.lm_parts, p.M, anchor, U,
+  const int parts = gate_w ? gated_parts(p) : p.lm_parts;
+  if (df::select_walk_smem(parts) <= 227 * 1024)  // merge fused with the walk
+    return cuda_status(df::launch_select_walk(p.bf16, w.part_val, w.part_id, w.part_ms, parts, p.M, anchor, U,
                                               V, g, p.B, p.T, p.K, p.R, p.V, p.greedy ? 1 : 0, cand_ids, cand_lp,
                                               lse, path_ids, path_idx, score, w.err, s));
   int32_t* ids = cand_ids ? cand_ids : w.cand_ids;
   float* lp = cand_lp ? cand_lp : w.cand_lp;
-  if ((st = run_merge(p, ids, lp, lse, w, s)) != DFLASH2_OK) return st;
+  if ((st = run_merge(p, ids, lp, lse, w, s, parts)) != DFLASH2_OK) return st;
   return run_walk(p, anchor, ids, lp, U, V, g, path_ids, path_idx, score, w, s);
 }
 

@@ -10,12 +10,13 @@
 namespace df {
 
 // tcgen05 GEMM + top-K/lse partials (bf16). grid = n_rc * parts.
-// g16: 16-row box map of the gate matrix (any valid map when args.gate_cols == 0); vocab: the
-// ranked columns; gate_out [M, gate_cols] fp32 receives the gate columns.
+// g128 / g16: 128- and 16-row box maps of the gate matrix (any valid maps when
+// args.gate_cols == 0; g128 is used only when gate_cols >= 128); vocab: the ranked columns;
+// gate_out [M, gate_cols] fp32 receives the gate columns.
 cudaError_t launch_lmhead_topk_bf16(const CUtensorMap& a, const CUtensorMap& a_tail, const CUtensorMap& b128,
-                                    const CUtensorMap& b16, const CUtensorMap& g16, const TcGemmArgs& args,
-                                    int vocab, float* part_val, int32_t* part_id, float* part_ms,
-                                    float* gate_out, cudaStream_t s);
+                                    const CUtensorMap& b16, const CUtensorMap& g128, const CUtensorMap& g16,
+                                    const TcGemmArgs& args, int vocab, float* part_val, int32_t* part_id,
+                                    float* part_ms, float* gate_out, cudaStream_t s);
 
 // tcgen05 GEMM + conv-layer epilogue (bf16): y = mix(x) with taps = x * W^T.
 cudaError_t launch_conv_layer_bf16(const CUtensorMap& a, const CUtensorMap& a_tail, const CUtensorMap& b128,

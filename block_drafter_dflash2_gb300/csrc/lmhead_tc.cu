@@ -9,8 +9,8 @@ namespace df {
 namespace {
 template <class Epi>
 cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& a_tail, const CUtensorMap& b128,
-                        const CUtensorMap& b16, const CUtensorMap& g16, const TcGemmArgs& args,
-                        const typename Epi::Params& ep, cudaStream_t s) {
+                        const CUtensorMap& b16, const CUtensorMap& g128, const CUtensorMap& g16,
+                        const TcGemmArgs& args, const typename Epi::Params& ep, cudaStream_t s) {
   static unsigned char smem_done[64];
   cudaError_t e = smem_opt_in(reinterpret_cast<const void*>(tc_gemm_kernel<Epi>), smem_done);
   if (e != cudaSuccess) return e;
@@ -34,21 +34,21 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& a_tail, const C
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = args.cluster > 1 ? 2 : 1;
-  e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<Epi>, a, a_tail, b128, b16, g16, args, ep);
+  e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<Epi>, a, a_tail, b128, b16, g128, g16, args, ep);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 }  // namespace
 
 cudaError_t launch_lmhead_topk_bf16(const CUtensorMap& a, const CUtensorMap& a_tail, const CUtensorMap& b128,
-                                    const CUtensorMap& b16, const CUtensorMap& g16, const TcGemmArgs& args,
-                                    int vocab, float* part_val, int32_t* part_id, float* part_ms,
-                                    float* gate_out, cudaStream_t s) {
+                                    const CUtensorMap& b16, const CUtensorMap& g128, const CUtensorMap& g16,
+                                    const TcGemmArgs& args, int vocab, float* part_val, int32_t* part_id,
+                                    float* part_ms, float* gate_out, cudaStream_t s) {
   if (args.gate_cols > 0 && (args.gate_base < vocab || args.gate_base % 16 != 0 || gate_out == nullptr ||
-                             args.n_total != args.gate_base + args.gate_cols))
+                             args.n_total != vocab || args.parts < 2 || args.cluster != 1))
     return cudaErrorInvalidValue;
   EpiTopK::Params ep{part_val, part_id, part_ms, args.M, vocab, gate_out, args.gate_base, args.gate_cols};
-  return launch_gemm<EpiTopK>(a, a_tail, b128, b16, g16, args, ep, s);
+  return launch_gemm<EpiTopK>(a, a_tail, b128, b16, g128, g16, args, ep, s);
 }
 
 cudaError_t launch_conv_layer_bf16(const CUtensorMap& a, const CUtensorMap& a_tail, const CUtensorMap& b128,
@@ -56,7 +56,7 @@ cudaError_t launch_conv_layer_bf16(const CUtensorMap& a, const CUtensorMap& a_ta
                                    int raw, cudaStream_t s) {
   EpiConv::Params ep{reinterpret_cast<const __nv_bfloat16*>(x), reinterpret_cast<__nv_bfloat16*>(y), args.M,
                      args.K, T, raw};
-  return launch_gemm<EpiConv>(a, a_tail, b128, b16, b16, args, ep, s);
+  return launch_gemm<EpiConv>(a, a_tail, b128, b16, b128, b16, args, ep, s);
 }
 
 }  // namespace df

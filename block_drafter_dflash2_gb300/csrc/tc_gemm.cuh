@@ -20,10 +20,12 @@
 // stale data and only feed TMEM lanes no epilogue thread reads. TMEM holds two fp32
 // accumulators as wide as a tile, so the epilogue of tile t overlaps the MMAs of tile t+1.
 //
-// Gate columns: the LM-head launch can append the rows of a second matrix (the context gate's
-// [R, H] weights) as extra columns past the vocabulary; they are fetched from their own
-// tensor map in 16-row boxes, balanced over the partitions like any other column, and the
-// epilogue stores their fp32 values instead of ranking them.
+// Gate columns: the LM-head launch can add the rows of a second matrix (the context gate's
+// [R, H] weights) as extra columns past the vocabulary, numbered from gate_base. They form a
+// partition of their own, the last CTA's, fetched through the gate's own tensor maps, and the
+// vocabulary is balanced over the other partitions; so no tile straddles the two matrices (a
+// tile that did, fetched in 16-row boxes, measured 130 us slower). The epilogue stores the
+// gate columns' fp32 values instead of ranking them.
 #pragma once
 
 #include "ptx.cuh"
@@ -47,12 +49,21 @@ struct TileRange {
   int num_tiles;
 };
 
+DF_DEV bool is_gate_part(const TcGemmArgs& a, int part) { return a.gate_cols > 0 && part == a.parts - 1; }
+
 DF_DEV TileRange tile_range(const TcGemmArgs& a, int part) {
   TileRange r;
-  const int units = (a.n_total + 15) / 16;
-  r.u0 = (int)((int64_t)part * units / a.parts);
-  r.u1 = (int)((int64_t)(part + 1) * units / a.parts);
-  r.col_end = min(r.u1 * 16, a.n_total);
+  if (is_gate_part(a, part)) {
+    r.u0 = a.gate_base / 16;
+    r.u1 = r.u0 + (a.gate_cols + 15) / 16;
+    r.col_end = a.gate_base + a.gate_cols;
+  } else {
+    const int units = (a.n_total + 15) / 16;
+    const int vparts = a.gate_cols > 0 ? a.parts - 1 : a.parts;
+    r.u0 = (int)((int64_t)part * units / vparts);
+    r.u1 = (int)((int64_t)(part + 1) * units / vparts);
+    r.col_end = min(r.u1 * 16, a.n_total);
+  }
   r.num_tiles = (r.u1 - r.u0 + a.tile_units - 1) / a.tile_units;
   return r;
 }
@@ -83,8 +94,8 @@ template <class Epi>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_a_tail,
                    const __grid_constant__ CUtensorMap map_b128, const __grid_constant__ CUtensorMap map_b16,
-                   const __grid_constant__ CUtensorMap map_g16, const TcGemmArgs args,
-                   const typename Epi::Params ep) {
+                   const __grid_constant__ CUtensorMap map_g128, const __grid_constant__ CUtensorMap map_g16,
+                   const TcGemmArgs args, const typename Epi::Params ep) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(base);
@@ -133,7 +144,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tma_prefetch_desc(tail_chunk ? &map_a_tail : &map_a);
     tma_prefetch_desc(&map_b128);
     tma_prefetch_desc(&map_b16);
-    if (args.gate_cols > 0) tma_prefetch_desc(&map_g16);
+    if (is_gate_part(args, part)) {
+      tma_prefetch_desc(&map_g16);
+      if (args.gate_cols >= 128) tma_prefetch_desc(&map_g128);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -147,6 +161,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint64_t pol_a = l2_policy_evict_last();   // row tiles are re-read for every column tile
       const uint64_t pol_b = l2_policy_evict_first();  // column tiles (weights) stream through once
       const CUtensorMap* ma = tail_chunk ? &map_a_tail : &map_a;
+      // B: the vocabulary, or the gate matrix for the gate partition (its rows from gate_base)
+      const bool gate_part = is_gate_part(args, part);
+      const CUtensorMap* mb128 = gate_part ? &map_g128 : &map_b128;
+      const CUtensorMap* mb16 = gate_part ? &map_g16 : &map_b16;
+      const int row0 = gate_part ? args.gate_base : 0;
       // The rows are the previous kernel's output (launched as its programmatic dependent,
       // this kernel's prologue overlaps its end): wait for it before the first load.
       pdl_wait();
@@ -168,22 +187,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           uint8_t* sb = sa + sg.b_off;
           mbar_arrive_expect_tx(&full[stage], bytes);
           tma_load_2d(sa, ma, &full[stage], kb * kBK, rc * kBM, pol_a);
-          if (args.gate_cols > 0 && n0 + nu * 16 > args.gate_base) {
-            // a tile reaching the gate columns: 16-row boxes, each from its own matrix
-            for (int j = 0; j < nu; ++j) {
-              const int col = n0 + 16 * j;
-              if (col >= args.gate_base)
-                tma_load_2d(sb + j * 16 * kBK * 2, &map_g16, &full[stage], kb * kBK, col - args.gate_base, pol_b);
-              else
-                tma_load_2d(sb + j * 16 * kBK * 2, &map_b16, &full[stage], kb * kBK, col, pol_b);
-            }
-          } else if (CL == 1) {
+          if (CL == 1) {
             if (nu % 8 == 0) {
               for (int j = 0; j < nu / 8; ++j)
-                tma_load_2d(sb + j * 128 * kBK * 2, &map_b128, &full[stage], kb * kBK, n0 + 128 * j, pol_b);
+                tma_load_2d(sb + j * 128 * kBK * 2, mb128, &full[stage], kb * kBK, n0 - row0 + 128 * j, pol_b);
             } else {
               for (int j = 0; j < nu; ++j)
-                tma_load_2d(sb + j * 16 * kBK * 2, &map_b16, &full[stage], kb * kBK, n0 + 16 * j, pol_b);
+                tma_load_2d(sb + j * 16 * kBK * 2, mb16, &full[stage], kb * kBK, n0 - row0 + 16 * j, pol_b);
             }
           } else {
             // this CTA's share of the B tile, multicast into every CTA of the cluster

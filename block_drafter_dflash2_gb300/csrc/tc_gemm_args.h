@@ -16,9 +16,10 @@ struct TcGemmArgs {
   int cluster;      // 1; or n_rc (2, 4, 8): the row-chunk CTAs of a column range multicast its
                     // weight tiles to each other (supported, not chosen by the planner: slower)
   int32_t* err;  // device error word
-  // Extra columns from a second matrix (the context gate): columns [gate_base, gate_base +
-  // gate_cols) are rows 0.. of the map_g16 matrix, columns below gate_base rows of map_b.
-  // gate_base is a multiple of 16; gate_cols = 0: every column is from map_b.
+  // Extra columns from a second matrix (the context gate): with gate_cols > 0 the last of
+  // `parts` partitions holds columns [gate_base, gate_base + gate_cols), rows 0.. of the gate
+  // matrix, and the vocabulary [0, n_total) is split over the other parts - 1. gate_base is a
+  // multiple of 16 and >= n_total; gate_cols = 0: no gate partition.
   int gate_base = 0;
   int gate_cols = 0;
 };

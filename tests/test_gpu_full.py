@@ -57,3 +57,25 @@ def test_full_size_workload(config):
           f"small margins {rep['path_vs_oracle_mismatch_small_margin']}; end to end: same ids "
           f"{rep['e2e_rows_same_ids']:.3f}, same sets {rep['e2e_rows_same_set']:.3f}, same paths "
           f"{rep['e2e_paths_same']:.3f}, lse err {rep['e2e_lse_max_err']:.2e}")
+
+
+@pytest.mark.parametrize("config", [2, 4])
+def test_full_size_workload_gated(config):
+    # the context gate at full size: the gate rows formed in the LM-head pass over the whole
+    # vocabulary plus the 256 gate columns, the gated walk exact on the GPU's own candidates
+    # and gate rows, and the oracle end to end on sampled sequences
+    rc = synth.recipe(config)
+    sh = rc.shape
+    sh.gate = True
+    inp = synth.make_inputs(rc)
+    B, T, R = sh.batch, sh.block, sh.rank
+    g = P.run_tail(P.shape_of(sh), P.upload_inputs(inp), gated=True)
+    assert g["device_error"] == 0
+    assert g["gate"].shape == (B, T, R) and np.all(np.isfinite(g["gate"]))
+    P.check_walk(sh, inp["anchor"], inp["U"], inp["V"], g["cand_ids"], g["cand_lp"], g["path_idx"],
+                 g["path_ids"], g["score"], gate=g["gate"])
+    seqs = SAMPLES[config]
+    ref = O.draft_tail(inp, sh, seqs=seqs)
+    rep = P.check_tail(sh, inp, ref, g, seqs=seqs)
+    print(f"workload {config} gated: gate err {rep['gate_max_abs_err']:.2e}, paths differing at small margins "
+          f"{rep['path_vs_oracle_mismatch_small_margin']}, same paths {rep['e2e_paths_same']:.3f}")
