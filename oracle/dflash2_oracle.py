@@ -39,7 +39,9 @@ Readings where the pages are silent (each is a fixed choice, stated where used):
      head reads), gate_w [R, H]. The selector's +2.0M parameters of Table 2 fit one such
      [hidden x 256] map per embedding (3 x 2560 x 256 at the 4B target's hidden 2560).
   R9 the walk is a Viterbi (exact best path); the pages' greedy walk is kept as
-     ``greedy_walk`` for comparison.
+     ``greedy_walk`` for comparison; at temperature T > 0 a path is sampled from the same
+     scores (``sample_walk``: P(path) proportional to exp(score / T), forward filtering and
+     backward sampling, with the caller's uniform draws).
   R10 top-K order: logit descending, ties to the lower token id; Viterbi ties go
       to the lower candidate index.
   R12 storage: layer outputs are rounded to the input dtype (bf16 RNE or fp32);
@@ -325,6 +327,58 @@ def greedy_walk(cand_lp: np.ndarray, tau: np.ndarray):
             path[b, t] = j
         score[b] = d
     return path, score
+
+
+def sample_walk(cand_lp: np.ndarray, tau: np.ndarray, temperature: float, u: np.ndarray):
+    """A path drawn from the same scores at temperature T > 0 (the pages' sampling mode,
+    [P4] "同じスコアからサンプリング"): P(path) = exp(score(path) / T) / Z over the K^T paths of
+    the candidate lattice, score(path) = sum_t lp_t(j_t) + tau_t(j_{t-1}, j_t) as in ``viterbi``.
+
+    Forward filtering, then backward sampling, in float64:
+      alpha_0(j) = (lp_0(j) + tau_0(0, j)) / T,
+      alpha_t(j) = lp_t(j) / T + logsumexp_i (alpha_{t-1}(i) + tau_t(i, j) / T);
+      j_{T-1} ~ softmax_j alpha_{T-1}(j);  j_{t-1} ~ softmax_i (alpha_{t-1}(i) + tau_t(i, j_t) / T).
+    Each draw takes u[b, t] in [0, 1) (slot t's draw) and picks the smallest index whose cumulative
+    probability exceeds it (inverse CDF, candidates in index order).
+    Returns (path_idx [B,T] int32, logprob [B] float64 = log P(path), cdf_margin [B] float64 = the
+    smallest distance between a draw and a cumulative-probability boundary along the path)."""
+    B, T, K = cand_lp.shape
+    lp = cand_lp.astype(np.float64)
+    tt = tau.astype(np.float64)
+    inv_t = 1.0 / float(temperature)
+    path = np.zeros((B, T), dtype=np.int32)
+    logp = np.zeros(B)
+    margin = np.full(B, np.inf)
+
+    def lse(v):
+        m = np.max(v)
+        return m + np.log(np.sum(np.exp(v - m))) if np.isfinite(m) else m
+
+    def draw(logw, uu):
+        p = np.exp(logw - lse(logw))
+        c = np.cumsum(p)
+        k = int(np.searchsorted(c, uu, side="right"))
+        k = min(k, len(p) - 1)
+        near = np.min(np.abs(c[:-1] - uu)) if len(p) > 1 else np.inf
+        return k, float(np.log(p[k])), near
+
+    for b in range(B):
+        alpha = np.zeros((T, K))
+        alpha[0] = (lp[b, 0] + tt[b, 0, 0]) * inv_t
+        for t in range(1, T):
+            for j in range(K):
+                alpha[t, j] = lp[b, t, j] * inv_t + lse(alpha[t - 1] + tt[b, t, :, j] * inv_t)
+        j, lpj, near = draw(alpha[T - 1], float(u[b, T - 1]))
+        path[b, T - 1] = j
+        logp[b] += lpj
+        margin[b] = min(margin[b], near)
+        for t in range(T - 1, 0, -1):
+            i, lpi, near = draw(alpha[t - 1] + tt[b, t, :, j] * inv_t, float(u[b, t - 1]))
+            path[b, t - 1] = i
+            logp[b] += lpi
+            margin[b] = min(margin[b], near)
+            j = i
+    return path, logp, margin
 
 
 def brute_force_best(cand_lp: np.ndarray, tau: np.ndarray):

@@ -398,6 +398,78 @@ def test_viterbi_single_slot_and_exact_ties():
 # ---------------------------------------------------------------- whole tail
 
 
+# ---------------------------------------------------------------- sampling at T > 0
+
+
+def _lattice(seed, B=2, T=3, K=3):
+    rng = np.random.default_rng(seed)
+    lp = (-np.abs(rng.standard_normal((B, T, K)))).astype(np.float32)
+    tau = (rng.standard_normal((B, T, K, K)) * 0.7).astype(np.float32)
+    tau[:, 0] = tau[:, 0, :1]  # slot 0's predecessor is the anchor: one row, repeated
+    return lp, tau
+
+
+def test_sample_walk_logprob_is_score_over_temperature_minus_log_partition():
+    # P(path) = exp(score / T) / Z: the sampler's log-probability of the path it drew equals the
+    # brute-force value from all K^T paths
+    import itertools
+    lp, tau = _lattice(1)
+    B, T, K = lp.shape
+    rng = np.random.default_rng(2)
+    for temp in (0.5, 1.0, 3.0):
+        for _ in range(5):
+            u = rng.random((B, T))
+            path, logp, _ = O.sample_walk(lp, tau, temp, u)
+            for b in range(B):
+                scores = [O.path_score(lp[b:b + 1], tau[b:b + 1], np.asarray(c)[None])[0] / temp
+                          for c in itertools.product(range(K), repeat=T)]
+                logz = np.logaddexp.reduce(scores)
+                s = O.path_score(lp[b:b + 1], tau[b:b + 1], path[b:b + 1])[0] / temp
+                assert abs(logp[b] - (s - logz)) < 1e-9
+
+
+def test_sample_walk_frequencies_match_brute_force_distribution():
+    # inverse-CDF draws on a regular grid of u reproduce the path distribution
+    import itertools
+    lp, tau = _lattice(3, B=1, T=2, K=3)
+    temp = 0.8
+    paths = list(itertools.product(range(3), repeat=2))
+    scores = np.array([O.path_score(lp, tau, np.asarray(c)[None])[0] / temp for c in paths])
+    prob = np.exp(scores - np.logaddexp.reduce(scores))
+    n = 200
+    counts = {c: 0 for c in paths}
+    for a in range(n):
+        for c in range(n):
+            u = np.array([[(c + 0.5) / n, (a + 0.5) / n]])
+            p, _, _ = O.sample_walk(lp, tau, temp, u)
+            counts[tuple(int(x) for x in p[0])] += 1
+    freq = np.array([counts[c] for c in paths]) / n ** 2
+    assert np.abs(freq - prob).max() < 0.02
+
+
+def test_sample_walk_low_temperature_is_viterbi():
+    lp, tau = _lattice(5, B=3, T=4, K=4)
+    rng = np.random.default_rng(6)
+    vp, _ = O.viterbi(lp, tau)
+    for _ in range(5):
+        p, _, _ = O.sample_walk(lp, tau, 1e-4, rng.random((3, 4)) * 0.98 + 0.01)
+        assert np.array_equal(p, vp)
+
+
+def test_sample_walk_without_transitions_is_independent_softmax():
+    # tau = 0: each slot is drawn from softmax(lp_t / T) by inverse CDF, independently
+    lp, _ = _lattice(7, B=2, T=3, K=4)
+    tau = np.zeros((2, 3, 4, 4), np.float32)
+    u = np.array([[0.1, 0.5, 0.95], [0.7, 0.02, 0.33]])
+    temp = 1.5
+    p, _, _ = O.sample_walk(lp, tau, temp, u)
+    for b in range(2):
+        for t in range(3):
+            w = np.exp(lp[b, t].astype(np.float64) / temp)
+            c = np.cumsum(w / w.sum())
+            assert p[b, t] == int(np.searchsorted(c, u[b, t], side="right"))
+
+
 def test_tiny_fp32_workload_end_to_end_brute_force():
     rc = synth.recipe(1)
     sh = rc.shape
