@@ -102,6 +102,12 @@ def load(path: str = LIB_PATH):
     lib.dflash2_draft_tail_gated.argtypes = [sp, vp, vp, vp, vp, vp, vp, i32p, i32p, i32p, vp, i32p, vp, vp, vp,
                                              vp, sz, vp]
     lib.dflash2_draft_tail_gated.restype = st
+    f32 = ctypes.c_float
+    lib.dflash2_sample_walk.argtypes = [sp, i32p, i32p, vp, vp, vp, vp, f32, vp, i32p, i32p, vp, vp, sz, vp]
+    lib.dflash2_sample_walk.restype = st
+    lib.dflash2_draft_tail_sampled.argtypes = [sp, vp, vp, vp, vp, vp, vp, i32p, f32, vp, i32p, i32p, vp, i32p, vp,
+                                               vp, vp, vp, sz, vp]
+    lib.dflash2_draft_tail_sampled.restype = st
     lib.dflash2_read_device_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]
     lib.dflash2_read_device_error.restype = st
     lib.dflash2_status_string.argtypes = [st]
@@ -239,6 +245,29 @@ def draft_tail_gated(shape: Shape, hidden, lm_head, U, V, conv_w, gate_w, anchor
                                            _ptr(conv_w), _ptr(gate_w), _ptr(anchor), _ptr(path_ids),
                                            _ptr(path_idx), _ptr(score), _ptr(cand_ids), _ptr(cand_lp), _ptr(lse),
                                            _ptr(gate), wp, wn, _stream(stream)), "dflash2_draft_tail_gated")
+
+
+def sample_walk(shape: Shape, anchor, cand_ids, cand_lp, U, V, temperature, uniforms, path_ids, path_idx, score,
+                ws, gate=None, stream=None):
+    """dflash2_sample_walk: a path drawn at temperature > 0 with the caller's uniforms [B,T];
+    score receives log P(path)."""
+    wp, wn = _ws(ws)
+    _check(load().dflash2_sample_walk(ctypes.byref(shape), _ptr(anchor), _ptr(cand_ids), _ptr(cand_lp), _ptr(U),
+                                      _ptr(V), _ptr(gate), ctypes.c_float(temperature), _ptr(uniforms),
+                                      _ptr(path_ids), _ptr(path_idx), _ptr(score), wp, wn, _stream(stream)),
+           "dflash2_sample_walk")
+
+
+def draft_tail_sampled(shape: Shape, hidden, lm_head, U, V, conv_w, anchor, temperature, uniforms, path_ids,
+                       path_idx, score, ws, gate_w=None, cand_ids=None, cand_lp=None, lse=None, gate=None,
+                       stream=None):
+    """dflash2_draft_tail_sampled: the whole tail, the walk drawing a path at temperature > 0."""
+    wp, wn = _ws(ws)
+    _check(load().dflash2_draft_tail_sampled(ctypes.byref(shape), _ptr(hidden), _ptr(lm_head), _ptr(U), _ptr(V),
+                                             _ptr(conv_w), _ptr(gate_w), _ptr(anchor), ctypes.c_float(temperature),
+                                             _ptr(uniforms), _ptr(path_ids), _ptr(path_idx), _ptr(score),
+                                             _ptr(cand_ids), _ptr(cand_lp), _ptr(lse), _ptr(gate), wp, wn,
+                                             _stream(stream)), "dflash2_draft_tail_sampled")
 
 
 def read_device_error(ws, stream=None) -> int:

@@ -315,11 +315,14 @@ dflash2_status_t run_merge(const Plan& p, int32_t* ids, float* lp, float* lse, c
                                            p.K, ids, lp, lse ? lse : w.lse, s));
 }
 
+// uniforms [B, T] (nullptr: the Viterbi / greedy walk) and inv_temp: draw a path instead
 dflash2_status_t run_walk(const Plan& p, const int32_t* anchor, const int32_t* ids, const float* lp,
                           const void* U, const void* V, const float* gate, int32_t* path_ids, int32_t* path_idx,
-                          float* score, const Ws& w, cudaStream_t s) {
+                          float* score, const Ws& w, cudaStream_t s, const float* uniforms = nullptr,
+                          float inv_temp = 0.f) {
   return cuda_status(df::launch_transition_walk(p.bf16, anchor, ids, lp, U, V, gate, p.B, p.T, p.K, p.R, p.V,
-                                                p.greedy ? 1 : 0, path_ids, path_idx, score, w.err, s));
+                                                p.greedy ? 1 : 0, uniforms, inv_temp, path_ids, path_idx, score,
+                                                w.err, s));
 }
 
 // ---- scratch for dflash2_select_topk_noalloc: a fixed device array instead of a caller
@@ -464,16 +467,25 @@ dflash2_status_t dflash2_viterbi_gated(const dflash2_shape_t* shape, const int32
                                        const float* cand_lp, const void* U, const void* V, const float* gate,
                                        int32_t* path_ids, int32_t* path_idx, float* score, void* ws,
                                        size_t ws_bytes, void* stream) {
+  return dflash2_sample_walk(shape, anchor, cand_ids, cand_lp, U, V, gate, 0.f, nullptr, path_ids, path_idx, score,
+                             ws, ws_bytes, stream);
+}
+
+dflash2_status_t dflash2_sample_walk(const dflash2_shape_t* shape, const int32_t* anchor, const int32_t* cand_ids,
+                                     const float* cand_lp, const void* U, const void* V, const float* gate,
+                                     float temperature, const float* uniforms, int32_t* path_ids, int32_t* path_idx,
+                                     float* score, void* ws, size_t ws_bytes, void* stream) {
   Plan p;
   dflash2_status_t st = make_plan(shape, p);
   if (st != DFLASH2_OK) return st;
   if (!anchor || !cand_ids || !cand_lp || !U || !V || !path_ids || !path_idx || !score)
     return DFLASH2_ERR_INVALID_ARGUMENT;
   if (!aligned16(U) || !aligned16(V) || (gate && !aligned16(gate))) return DFLASH2_ERR_INVALID_ARGUMENT;
+  if (uniforms && !(temperature > 0.f && temperature < 1e30f)) return DFLASH2_ERR_INVALID_ARGUMENT;
   Ws w;
   if ((st = check_ws(p, ws, ws_bytes, w)) != DFLASH2_OK) return st;
   return run_walk(p, anchor, cand_ids, cand_lp, U, V, gate, path_ids, path_idx, score, w,
-                  static_cast<cudaStream_t>(stream));
+                  static_cast<cudaStream_t>(stream), uniforms, uniforms ? 1.f / temperature : 0.f);
 }
 
 dflash2_status_t dflash2_draft_tail(const dflash2_shape_t* shape, const void* hidden, const void* lm_head,
@@ -489,6 +501,16 @@ dflash2_status_t dflash2_draft_tail_gated(const dflash2_shape_t* shape, const vo
                                           const int32_t* anchor, int32_t* path_ids, int32_t* path_idx, float* score,
                                           int32_t* cand_ids, float* cand_lp, float* lse, float* gate,
                                           void* ws, size_t ws_bytes, void* stream) {
+  return dflash2_draft_tail_sampled(shape, hidden, lm_head, U, V, conv_w, gate_w, anchor, 0.f, nullptr, path_ids,
+                                    path_idx, score, cand_ids, cand_lp, lse, gate, ws, ws_bytes, stream);
+}
+
+dflash2_status_t dflash2_draft_tail_sampled(const dflash2_shape_t* shape, const void* hidden, const void* lm_head,
+                                            const void* U, const void* V, const void* conv_w, const void* gate_w,
+                                            const int32_t* anchor, float temperature, const float* uniforms,
+                                            int32_t* path_ids, int32_t* path_idx, float* score, int32_t* cand_ids,
+                                            float* cand_lp, float* lse, float* gate, void* ws, size_t ws_bytes,
+                                            void* stream) {
   Plan p;
   dflash2_status_t st = make_plan(shape, p);
   if (st != DFLASH2_OK) return st;
@@ -498,10 +520,12 @@ dflash2_status_t dflash2_draft_tail_gated(const dflash2_shape_t* shape, const vo
       (conv_w && !aligned16(conv_w)) || (gate_w && !aligned16(gate_w)))
     return DFLASH2_ERR_INVALID_ARGUMENT;
   if (gate && !aligned16(gate)) return DFLASH2_ERR_INVALID_ARGUMENT;
+  if (uniforms && !(temperature > 0.f && temperature < 1e30f)) return DFLASH2_ERR_INVALID_ARGUMENT;
   if (gate_w && !p.bf16) return DFLASH2_ERR_UNSUPPORTED;
   Ws w;
   if ((st = check_ws(p, ws, ws_bytes, w)) != DFLASH2_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const float inv_temp = uniforms ? 1.f / temperature : 0.f;
   // z: the last conv layer's output lands in conv0/conv1 (never the caller's hidden)
   const void* z = hidden;
   if (p.NL > 0) {
@@ -517,12 +541,12 @@ dflash2_status_t dflash2_draft_tail_gated(const dflash2_shape_t* shape, const vo
   const int parts = gate_w ? gated_parts(p) : p.lm_parts;
   if (df::select_walk_smem(parts) <= 227 * 1024)  // merge fused with the walk
     return cuda_status(df::launch_select_walk(p.bf16, w.part_val, w.part_id, w.part_ms, parts, p.M, anchor, U,
-                                              V, g, p.B, p.T, p.K, p.R, p.V, p.greedy ? 1 : 0, cand_ids, cand_lp,
-                                              lse, path_ids, path_idx, score, w.err, s));
+                                              V, g, p.B, p.T, p.K, p.R, p.V, p.greedy ? 1 : 0, uniforms, inv_temp,
+                                              cand_ids, cand_lp, lse, path_ids, path_idx, score, w.err, s));
   int32_t* ids = cand_ids ? cand_ids : w.cand_ids;
   float* lp = cand_lp ? cand_lp : w.cand_lp;
   if ((st = run_merge(p, ids, lp, lse, w, s, parts)) != DFLASH2_OK) return st;
-  return run_walk(p, anchor, ids, lp, U, V, g, path_ids, path_idx, score, w, s);
+  return run_walk(p, anchor, ids, lp, U, V, g, path_ids, path_idx, score, w, s, uniforms, inv_temp);
 }
 
 dflash2_status_t dflash2_read_device_error(void* ws, void* stream, int32_t* code_out) {

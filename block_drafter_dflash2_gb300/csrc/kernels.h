@@ -77,13 +77,16 @@ size_t select_walk_smem(int parts);
 cudaError_t launch_select_walk(bool bf16, const float* part_val, const int32_t* part_id, const float* part_ms,
                                int parts, int M, const int32_t* anchor, const void* U, const void* V,
                                const float* gate, int B, int T, int K, int R, int vocab, int greedy,
-                               int32_t* cand_ids, float* cand_lp, float* lse, int32_t* path_ids, int32_t* path_idx,
-                               float* score, int32_t* err, cudaStream_t s);
+                               const float* uniforms, float inv_temp, int32_t* cand_ids, float* cand_lp,
+                               float* lse, int32_t* path_ids, int32_t* path_idx, float* score, int32_t* err,
+                               cudaStream_t s);
 
-// Transition tiles + Viterbi / greedy walk, one CTA per sequence.
+// Transition tiles + Viterbi / greedy walk, one CTA per sequence. uniforms [B, T] (nullptr: no
+// sampling) and inv_temp: draw a path at temperature 1 / inv_temp instead.
 cudaError_t launch_transition_walk(bool bf16, const int32_t* anchor, const int32_t* cand_ids,
                                    const float* cand_lp, const void* U, const void* V, const float* gate, int B,
-                                   int T, int K, int R, int vocab, int greedy, int32_t* path_ids, int32_t* path_idx,
-                                   float* score, int32_t* err, cudaStream_t s);
+                                   int T, int K, int R, int vocab, int greedy, const float* uniforms,
+                                   float inv_temp, int32_t* path_ids, int32_t* path_idx, float* score, int32_t* err,
+                                   cudaStream_t s);
 
 }  // namespace df

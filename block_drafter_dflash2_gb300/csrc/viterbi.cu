@@ -11,6 +11,10 @@
 // lp_t(j), and keeps the back-pointer; a shuffle arg-max (lowest index on ties) picks the
 // final state and lane 0 reads the path back.
 //
+// Sampling (optional, temperature > 0): instead of the best path, warp 0 draws one from
+// P(path) ~ exp(score / temperature) by forward filtering (log-sum-exp over the previous
+// candidates) and backward inverse-CDF draws on the caller's uniforms.
+//
 // Context gate (optional): tau_t(i, j) = sum_r U[prev_i][r] g_t[r] V[cur_j][r] with g_t the gate
 // of slot t (fp32, [B*T, R]). The warp that builds tile t scales its staged V rows by g_t and
 // rounds them to bf16 before the MMA (one rounding of V[cur_j][r] g_t[r]; fp32 embeddings keep
@@ -41,8 +45,16 @@ struct SmemWalk {
   int32_t ids[kMaxT][kKP];
   float lp[kMaxT][kKP];
   float tau[kMaxT][kKP][kKP];
+  float alpha[kMaxT][kKP];  // sampling: forward log-weights
   int8_t bp[kMaxT][kKP];
   int32_t anchor;
+};
+
+// Sampling parameters of the walk: u == nullptr is the Viterbi / greedy walk; otherwise a path
+// is drawn at temperature 1 / inv_temp with the uniforms u [B, T] (slot t's draw in u[b, t]).
+struct SampleArgs {
+  const float* u;
+  float inv_temp;
 };
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
@@ -216,13 +228,86 @@ __device__ void build_tiles(SmemWalk& sw, int T, int R, const void* Uv, const vo
   }
 }
 
-// The walk for sequence b on warp 0 (the other warps return before calling it).
-__device__ void walk_warp0(SmemWalk& sw, int b, int T, int K, int greedy, int32_t* __restrict__ path_ids,
-                           int32_t* __restrict__ path_idx, float* __restrict__ score) {
+// One inverse-CDF draw on warp 0: lane i < K holds the log-weight lw (-inf elsewhere); returns
+// the smallest index whose cumulative weight exceeds u times the total (index order), and the
+// log of its probability. Every lane returns the same values.
+__device__ __forceinline__ int draw_index(float lw, int K, float u, float& logp) {
+  const int lane = threadIdx.x & 31;
+  float m = lw;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const float w = lane < K ? expf(lw - m) : 0.f;
+  float c = w;  // inclusive prefix sum over lanes
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, c, o);
+    if (lane >= o) c += y;
+  }
+  const float total = __shfl_sync(0xffffffffu, c, 31);
+  const uint32_t above = __ballot_sync(0xffffffffu, lane < K && c > u * total);
+  const int k = above ? (__ffs(above) - 1) : K - 1;
+  const float wk = __shfl_sync(0xffffffffu, w, k);
+  logp = logf(wk / total);
+  return k;
+}
+
+// Forward filtering and backward sampling on warp 0 (fp32): P(path) = exp(score(path) * inv_temp)
+// / Z. alpha_0(j) = (lp_0(j) + tau_0(0, j)) inv_temp; alpha_t(j) = lp_t(j) inv_temp +
+// logsumexp_i (alpha_{t-1}(i) + tau_t(i, j) inv_temp). Then j_{T-1} ~ alpha_{T-1} and
+// j_{t-1} ~ alpha_{t-1}(i) + tau_t(i, j_t) inv_temp, each by inverse CDF on u[b, t]. score[b]
+// receives log P(path).
+__device__ void sample_warp0(SmemWalk& sw, int b, int T, int K, const SampleArgs& sa, int32_t* __restrict__ path_ids,
+                             int32_t* __restrict__ path_idx, float* __restrict__ score) {
   const int lane = threadIdx.x & 31;
   const int j = lane;
   const bool live = j < K;
-  if (!greedy) {
+  const float it = sa.inv_temp;
+  __shared__ float ash[kKP];
+  float a = live ? (sw.lp[0][j] + sw.tau[0][0][j]) * it : -INFINITY;
+  if (lane < kKP) sw.alpha[0][lane] = a;
+  for (int t = 1; t < T; ++t) {
+    if (lane < kKP) ash[lane] = a;
+    __syncwarp();
+    if (live) {
+      float m = -INFINITY;
+      for (int i = 0; i < K; ++i) m = fmaxf(m, ash[i] + sw.tau[t][i][j] * it);
+      float s = 0.f;
+      for (int i = 0; i < K; ++i) s += expf(ash[i] + sw.tau[t][i][j] * it - m);
+      a = sw.lp[t][j] * it + (m + logf(s));
+    }
+    if (lane < kKP) sw.alpha[t][lane] = a;
+    __syncwarp();
+  }
+  const float* u = sa.u + (size_t)b * T;
+  float lp_sum = 0.f, lpk;
+  int cj = draw_index(live ? sw.alpha[T - 1][j] : -INFINITY, K, u[T - 1], lpk);
+  lp_sum += lpk;
+  if (lane == 0) {
+    path_idx[(size_t)b * T + T - 1] = cj;
+    path_ids[(size_t)b * T + T - 1] = sw.ids[T - 1][cj];
+  }
+  for (int t = T - 1; t > 0; --t) {
+    const float lw = live ? sw.alpha[t - 1][j] + sw.tau[t][j][cj] * it : -INFINITY;
+    cj = draw_index(lw, K, u[t - 1], lpk);
+    lp_sum += lpk;
+    if (lane == 0) {
+      path_idx[(size_t)b * T + t - 1] = cj;
+      path_ids[(size_t)b * T + t - 1] = sw.ids[t - 1][cj];
+    }
+  }
+  if (lane == 0) score[b] = lp_sum;
+}
+
+// The walk for sequence b on warp 0 (the other warps return before calling it).
+__device__ void walk_warp0(SmemWalk& sw, int b, int T, int K, int greedy, const SampleArgs& sa,
+                           int32_t* __restrict__ path_ids, int32_t* __restrict__ path_idx,
+                           float* __restrict__ score) {
+  const int lane = threadIdx.x & 31;
+  const int j = lane;
+  const bool live = j < K;
+  if (sa.u) {
+    sample_warp0(sw, b, T, K, sa, path_ids, path_idx, score);
+  } else if (!greedy) {
     // Viterbi in fp32: delta_0 = lp_0 + tau_0(0, j); delta_t = lp_t + max_i (delta_{t-1}(i) + tau_t(i, j)).
     // delta(i) is read back from shared memory by every lane (a broadcast), so the inner
     // loop has no shuffle latency in it.
@@ -299,8 +384,8 @@ __global__ void __launch_bounds__(32 * kWarps)
     transition_walk_kernel(const int32_t* __restrict__ anchor, const int32_t* __restrict__ cand_ids,
                            const float* __restrict__ cand_lp, const void* __restrict__ Uv,
                            const void* __restrict__ Vv, const float* __restrict__ gate, int T, int K, int R,
-                           int vocab, int greedy, int32_t* __restrict__ path_ids, int32_t* __restrict__ path_idx,
-                           float* __restrict__ score, int32_t* err) {
+                           int vocab, int greedy, SampleArgs sa, int32_t* __restrict__ path_ids,
+                           int32_t* __restrict__ path_idx, float* __restrict__ score, int32_t* err) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   SmemWalk& sw = *reinterpret_cast<SmemWalk*>(smem_raw);
   __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(smem_raw + ((sizeof(SmemWalk) + 127) & ~size_t(127)));
@@ -321,7 +406,7 @@ __global__ void __launch_bounds__(32 * kWarps)
   build_tiles<kBf16>(sw, T, R, Uv, Vv, gate ? gate + (size_t)b * T * R : nullptr, stage);
   __syncthreads();
   if ((threadIdx.x >> 5) != 0) return;
-  walk_warp0(sw, b, T, K, greedy, path_ids, path_idx, score);
+  walk_warp0(sw, b, T, K, greedy, sa, path_ids, path_idx, score);
 }
 
 // Bytes of one warp's merge staging: values and ids [parts][16], (max, sum) [parts], heads.
@@ -344,7 +429,7 @@ __global__ void __launch_bounds__(32 * kWarps)
                        const float2* __restrict__ part_ms, int parts, int M, const int32_t* __restrict__ anchor,
                        const void* __restrict__ Uv, const void* __restrict__ Vv, const float* __restrict__ gate,
                        int T, int K, int R, int vocab,
-                       int greedy, int32_t* __restrict__ cand_ids, float* __restrict__ cand_lp,
+                       int greedy, SampleArgs sa, int32_t* __restrict__ cand_ids, float* __restrict__ cand_lp,
                        float* __restrict__ lse_out, int32_t* __restrict__ path_ids, int32_t* __restrict__ path_idx,
                        float* __restrict__ score, int32_t* err) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -460,7 +545,7 @@ __global__ void __launch_bounds__(32 * kWarps)
     __syncthreads();
   }
   if (warp != 0) return;
-  walk_warp0(sw, b, T, K, greedy, path_ids, path_idx, score);
+  walk_warp0(sw, b, T, K, greedy, sa, path_ids, path_idx, score);
 }
 
 constexpr size_t kWalkStageBytes = (size_t)kWarps * 2 * kKP * kRowPad * sizeof(__nv_bfloat16);
@@ -475,8 +560,10 @@ size_t select_walk_smem(int parts) {
 cudaError_t launch_select_walk(bool bf16, const float* part_val, const int32_t* part_id, const float* part_ms,
                                int parts, int M, const int32_t* anchor, const void* U, const void* V,
                                const float* gate, int B, int T, int K, int R, int vocab, int greedy,
-                               int32_t* cand_ids, float* cand_lp, float* lse, int32_t* path_ids, int32_t* path_idx,
-                               float* score, int32_t* err, cudaStream_t s) {
+                               const float* uniforms, float inv_temp, int32_t* cand_ids, float* cand_lp,
+                               float* lse, int32_t* path_ids, int32_t* path_idx, float* score, int32_t* err,
+                               cudaStream_t s) {
+  const SampleArgs sa{uniforms, inv_temp};
   if (T > kMaxT || K > kKP) return cudaErrorInvalidValue;
   const size_t smem = select_walk_smem(parts);
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
@@ -498,14 +585,14 @@ cudaError_t launch_select_walk(bool bf16, const float* part_val, const int32_t* 
     e = smem_opt_in(reinterpret_cast<const void*>(select_walk_kernel<true>), smem_done);
     if (e != cudaSuccess) return e;
     e = cudaLaunchKernelEx(&cfg, select_walk_kernel<true>, part_val, part_id, ms, parts, M, anchor, U, V, gate, T, K,
-                           R, vocab, greedy, cand_ids, cand_lp, lse, path_ids, path_idx, score, err);
+                           R, vocab, greedy, sa, cand_ids, cand_lp, lse, path_ids, path_idx, score, err);
     if (e != cudaSuccess) return e;
   } else {
     static unsigned char smem_done[64];
     e = smem_opt_in(reinterpret_cast<const void*>(select_walk_kernel<false>), smem_done);
     if (e != cudaSuccess) return e;
     e = cudaLaunchKernelEx(&cfg, select_walk_kernel<false>, part_val, part_id, ms, parts, M, anchor, U, V, gate, T,
-                           K, R, vocab, greedy, cand_ids, cand_lp, lse, path_ids, path_idx, score, err);
+                           K, R, vocab, greedy, sa, cand_ids, cand_lp, lse, path_ids, path_idx, score, err);
     if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
@@ -513,8 +600,10 @@ cudaError_t launch_select_walk(bool bf16, const float* part_val, const int32_t* 
 
 cudaError_t launch_transition_walk(bool bf16, const int32_t* anchor, const int32_t* cand_ids,
                                    const float* cand_lp, const void* U, const void* V, const float* gate, int B,
-                                   int T, int K, int R, int vocab, int greedy, int32_t* path_ids, int32_t* path_idx,
-                                   float* score, int32_t* err, cudaStream_t s) {
+                                   int T, int K, int R, int vocab, int greedy, const float* uniforms,
+                                   float inv_temp, int32_t* path_ids, int32_t* path_idx, float* score, int32_t* err,
+                                   cudaStream_t s) {
+  const SampleArgs sa{uniforms, inv_temp};
   if (T > kMaxT || K > kKP) return cudaErrorInvalidValue;
   const size_t base = (sizeof(SmemWalk) + 127) & ~size_t(127);
   const size_t smem = base + (bf16 ? kWalkStageBytes : 0);
@@ -524,13 +613,13 @@ cudaError_t launch_transition_walk(bool bf16, const int32_t* anchor, const int32
     e = smem_opt_in(reinterpret_cast<const void*>(transition_walk_kernel<true>), smem_done);
     if (e != cudaSuccess) return e;
     transition_walk_kernel<true><<<B, 32 * kWarps, smem, s>>>(anchor, cand_ids, cand_lp, U, V, gate, T, K, R,
-                                                               vocab, greedy, path_ids, path_idx, score, err);
+                                                               vocab, greedy, sa, path_ids, path_idx, score, err);
   } else {
     static unsigned char smem_done[64];
     e = smem_opt_in(reinterpret_cast<const void*>(transition_walk_kernel<false>), smem_done);
     if (e != cudaSuccess) return e;
     transition_walk_kernel<false><<<B, 32 * kWarps, smem, s>>>(anchor, cand_ids, cand_lp, U, V, gate, T, K, R,
-                                                                vocab, greedy, path_ids, path_idx, score, err);
+                                                                vocab, greedy, sa, path_ids, path_idx, score, err);
   }
   return cudaGetLastError();
 }

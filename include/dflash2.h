@@ -194,6 +194,25 @@ dflash2_status_t dflash2_viterbi_gated(const dflash2_shape_t* shape, const int32
                                        int32_t* path_ids, int32_t* path_idx, float* score,
                                        void* ws, size_t ws_bytes, void* stream);
 
+/* A path sampled at temperature T > 0 instead of the best one ("DFlash 2: keeping drafts
+ * parallel", section "軽量パスセレクター": the walk can also sample from the same scores):
+ * P(path) = exp(score(path) / T) / Z over the K^T paths, score(path) as for dflash2_viterbi
+ * (with the context gate when gate is non-NULL, as in dflash2_viterbi_gated). Forward filtering
+ * in fp32, alpha_0(j) = (lp_0(j) + tau_0(j)) / T, alpha_t(j) = lp_t(j) / T +
+ * logsumexp_i (alpha_{t-1}(i) + tau_t(i, j) / T); then backward draws: j_{T-1} ~ softmax(alpha_{T-1}),
+ * j_{t-1} ~ softmax_i (alpha_{t-1}(i) + tau_t(i, j_t) / T), each the smallest candidate index
+ * whose cumulative probability exceeds uniforms[b, t] (slot t's draw, in [0, 1)).
+ *   temperature > 0 (finite); uniforms [B, T] fp32 device: the caller's random numbers
+ *   (the library draws none, so a result is reproducible from its inputs)
+ *   score [B] fp32 receives log P(path) of the drawn path.
+ * uniforms NULL: the Viterbi / greedy walk (temperature ignored). */
+dflash2_status_t dflash2_sample_walk(const dflash2_shape_t* shape, const int32_t* anchor,
+                                     const int32_t* cand_ids, const float* cand_lp,
+                                     const void* U, const void* V, const float* gate,
+                                     float temperature, const float* uniforms,
+                                     int32_t* path_ids, int32_t* path_idx, float* score,
+                                     void* ws, size_t ws_bytes, void* stream);
+
 /* The whole tail in one call: conv -> LM head top-K + lse -> transitions + walk.
  *   hidden [B, T, H], lm_head [V, H], U/V [V, R], conv_w [NL, 2H/16, H], anchor [B]
  *   path_ids, path_idx [B, T] int32; score [B] fp32
@@ -213,6 +232,16 @@ dflash2_status_t dflash2_draft_tail_gated(const dflash2_shape_t* shape, const vo
                                           const int32_t* anchor, int32_t* path_ids, int32_t* path_idx,
                                           float* score, int32_t* cand_ids, float* cand_lp, float* lse,
                                           float* gate, void* ws, size_t ws_bytes, void* stream);
+
+/* dflash2_draft_tail_gated with the walk sampling at temperature T > 0 from the caller's
+ * uniforms [B, T] (as dflash2_sample_walk; score receives log P(path)); gate_w may be NULL
+ * (no context gate); uniforms NULL is dflash2_draft_tail_gated. */
+dflash2_status_t dflash2_draft_tail_sampled(const dflash2_shape_t* shape, const void* hidden, const void* lm_head,
+                                            const void* U, const void* V, const void* conv_w, const void* gate_w,
+                                            const int32_t* anchor, float temperature, const float* uniforms,
+                                            int32_t* path_ids, int32_t* path_idx, float* score,
+                                            int32_t* cand_ids, float* cand_lp, float* lse, float* gate,
+                                            void* ws, size_t ws_bytes, void* stream);
 
 /* Synchronises `stream`, returns the workspace's device error word in *code_out
  * (a DFLASH2_DEVERR_* bit set; 0 = none) and clears it. Returns DFLASH2_OK, or

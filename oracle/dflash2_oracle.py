@@ -381,6 +381,21 @@ def sample_walk(cand_lp: np.ndarray, tau: np.ndarray, temperature: float, u: np.
     return path, logp, margin
 
 
+def log_partition(cand_lp: np.ndarray, tau: np.ndarray, temperature: float) -> np.ndarray:
+    """log Z per sequence at temperature T: log sum over the K^T paths of exp(score(path) / T),
+    by the forward recursion of ``sample_walk`` in float64 (logsumexp of the last alpha)."""
+    B, T, K = cand_lp.shape
+    lp = cand_lp.astype(np.float64)
+    tt = tau.astype(np.float64)
+    out = np.zeros(B)
+    for b in range(B):
+        a = (lp[b, 0] + tt[b, 0, 0]) / temperature
+        for t in range(1, T):
+            a = lp[b, t] / temperature + np.logaddexp.reduce(a[:, None] + tt[b, t] / temperature, axis=0)
+        out[b] = np.logaddexp.reduce(a)
+    return out
+
+
 def brute_force_best(cand_lp: np.ndarray, tau: np.ndarray):
     """Enumerate all K^T paths of each sequence (tiny K, T only); float64 scores.
     Returns (path_idx [B,T] of the maximum, score [B]); the first path in

@@ -428,6 +428,17 @@ def test_sample_walk_logprob_is_score_over_temperature_minus_log_partition():
                 assert abs(logp[b] - (s - logz)) < 1e-9
 
 
+def test_log_partition_is_brute_force():
+    import itertools
+    lp, tau = _lattice(4, B=2, T=3, K=3)
+    for temp in (0.7, 2.0):
+        z = O.log_partition(lp, tau, temp)
+        for b in range(2):
+            scores = [O.path_score(lp[b:b + 1], tau[b:b + 1], np.asarray(c)[None])[0] / temp
+                      for c in itertools.product(range(3), repeat=3)]
+            assert abs(z[b] - np.logaddexp.reduce(scores)) < 1e-9
+
+
 def test_sample_walk_frequencies_match_brute_force_distribution():
     # inverse-CDF draws on a regular grid of u reproduce the path distribution
     import itertools
