@@ -145,6 +145,12 @@ def make_workload(config: int):
     return rc, inp
 
 
+def synth_uniforms(B: int, T: int):
+    """Seeded uniform draws [B, T] in [0, 1) for the sampling walk."""
+    import synth
+    return synth.uniform(7, 40, B * T).reshape(B, T)
+
+
 def hidden_for_batch(rc, batch: int, lm_head):
     """Hidden rows for another batch size with the same recipe (weights shared)."""
     import synth
@@ -390,6 +396,24 @@ def run_ours(args, rank, world, local_rank):
         extra["B=1 gated"] = {"us_per_call": round(usg, 2), "blocks_per_s": round(B / (usg * 1e-6), 1),
                               "tail_roofline_frac": round(tail_roofline_us(sh, M, bw, tf) / usg, 4),
                               "over_ungated_us": round(usg - total_ms / args.steps * 1e3, 2)}
+
+        # and with the walk sampling a path at temperature 1 (fixed seeded uniforms)
+        u_d = up(np.asarray(synth_uniforms(B, T), dtype=np.float32))
+
+        def call_s():
+            df2.draft_tail_sampled(shape, d["hidden"], d["lm_head"], d["U"], d["V"], d["conv_w"], d["anchor"], 1.0,
+                                   u_d, out["pid"], out["pix"], out["score"], ws, stream=stream)
+        with torch.cuda.stream(stream):
+            call_s()
+        torch.cuda.synchronize(dev)
+        assert df2.read_device_error(ws, stream) == 0
+        gs = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gs, stream=stream):
+            call_s()
+        mss = timed(gs.replay, args.steps, 3)
+        uss = statistics.mean(mss) * 1e3
+        extra["B=1 sampled T=1"] = {"us_per_call": round(uss, 2), "blocks_per_s": round(B / (uss * 1e-6), 1),
+                                    "over_viterbi_us": round(uss - total_ms / args.steps * 1e3, 2)}
 
     us = total_ms / args.steps * 1e3
     lm_us = statistics.mean(lm_ms) * 1e3
