@@ -30,7 +30,11 @@ Readings where the pages are silent (each is a fixed choice, stated where used):
   R4 layers are chained directly, with no residual, norm or activation between them
      and no norm before the LM head.
   R5 causal within the block, x[-1] = 0, sequences independent.
-  R6 all `block` rows are slots; the anchor is the predecessor of slot 0.
+  R6 all `block` rows are slots; the anchor is the predecessor of slot 0. The other reading
+     (first_slot = 1): row 0 of each block is the anchor's own position (the block is 1 +
+     the speculative tokens [P3]); its hidden row goes through the conv with the others, so the
+     slots see it, and the candidates and the walk cover rows 1..block-1, starting from the
+     anchor token.
   R7 per-slot score = log-softmax of the head's logits (this library's contract); the
      pages' raw-logit score gives the same path (per-slot constants cancel).
   R8 the context gate H(h_t) is taken as all-ones by default; with the gate on, H is a
@@ -436,12 +440,16 @@ def draft_tail(inp: dict, shape, seqs=None, row_block: int = 64) -> dict:
 
 def select_from_z(z: np.ndarray, inp: dict, shape, seqs, row_block: int = 64) -> dict:
     """The tail after the conv, on given conv outputs z [b, T, H] of the listed sequences:
-    logits, lse, top-K, transitions from those sequences' anchors, Viterbi and margins."""
-    T, H, K = shape.block, shape.hidden, shape.top_k
+    logits, lse, top-K, transitions from those sequences' anchors, Viterbi and margins.
+    With shape.first_slot = 1 (R6) the slots are rows 1..T-1 and every per-slot output has
+    T-1 slots."""
+    H, K = shape.hidden, shape.top_k
+    first = int(getattr(shape, "first_slot", 0))
+    T = shape.block - first
     seqs = list(seqs)
     anchor = np.asarray(inp["anchor"])[seqs]
     nb = len(seqs)
-    rows = np.asarray(z).reshape(nb * T, H)
+    rows = np.asarray(z)[:, first:, :].reshape(nb * T, H)
     M = rows.shape[0]
     ids = np.empty((M, K), dtype=np.int32)
     vals = np.empty((M, K), dtype=np.float32)

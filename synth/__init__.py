@@ -142,6 +142,7 @@ class Shape:
     dtype: str = "bf16"  # 'bf16' or 'f32'
     taps: str = "softmax"  # 'softmax' (default) or 'raw'
     gate: bool = False     # context gate H(h_t) in the transition scores
+    first_slot: int = 0    # 1: row 0 of each block is the anchor's position, slots are rows 1..block-1
 
     @property
     def rows(self) -> int:

@@ -481,6 +481,31 @@ def test_sample_walk_without_transitions_is_independent_softmax():
             assert p[b, t] == int(np.searchsorted(c, u[b, t], side="right"))
 
 
+def test_first_slot_reading_selects_rows_after_the_anchor_row():
+    # first_slot = 1: the conv runs over all block rows (the anchor row included, so slot 1 sees
+    # it), and the selection is the all-slots selection of rows 1..block-1 with the same anchor
+    rc = synth.scaled_recipe(synth.recipe(2), batch=2, block=5, hidden=64, vocab=500, rank=32, layers=2)
+    sh = rc.shape
+    inp = synth.make_inputs(rc)
+    sh1 = synth.Shape(**{**sh.__dict__, "first_slot": 1})
+    out1 = O.draft_tail(inp, sh1)
+    assert out1["path_idx"].shape == (2, 4) and out1["cand_ids"].shape == (2, 4, sh.top_k)
+    z = O.conv_chain(inp["hidden"], inp["conv_w"], sh.dtype, 16)
+    assert np.array_equal(O.widen(out1["z"]), O.widen(z))
+    sh0 = synth.Shape(**{**sh.__dict__, "block": 4})
+    out0 = O.select_from_z(z[:, 1:], inp, sh0, [0, 1])
+    for k in ("cand_ids", "cand_lp", "path_idx", "path_ids", "score"):
+        assert np.array_equal(out1[k], out0[k]), k
+    # the anchor row matters: changing it changes slot 1's conv output
+    h2 = inp["hidden"].copy()
+    h2[:, 0] = O.round_bf16(-O.widen(h2[:, 0])) if sh.dtype == "bf16" else -h2[:, 0]
+    z2 = O.conv_chain(h2, inp["conv_w"], sh.dtype, 16)
+    assert not np.array_equal(O.widen(z2[:, 1]), O.widen(z[:, 1]))
+    # and the walk over the 4 slots is the brute-force best path
+    bp, _ = O.brute_force_best(out1["cand_lp"], out1["tau"])
+    assert np.array_equal(bp, out1["path_idx"])
+
+
 def test_tiny_fp32_workload_end_to_end_brute_force():
     rc = synth.recipe(1)
     sh = rc.shape
