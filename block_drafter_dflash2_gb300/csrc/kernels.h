@@ -73,20 +73,22 @@ cudaError_t launch_topk_merge(const float* part_val, const int32_t* part_id, con
 // (the whole-tail call); cand_ids / cand_lp / lse may be null. Needs select_walk_smem(parts)
 // bytes of shared memory (at most 227 KB).
 size_t select_walk_smem(int parts);
-// gate: [B*T, R] fp32 context gate of every slot, or nullptr (no gate).
+// T slots per sequence at rows first .. first+T-1 of the sequence's rows_per_seq LM-head rows
+// (per-slot outputs); gate: [B*rows_per_seq, R] fp32 context gate of every row, or nullptr.
 cudaError_t launch_select_walk(bool bf16, const float* part_val, const int32_t* part_id, const float* part_ms,
                                int parts, int M, const int32_t* anchor, const void* U, const void* V,
-                               const float* gate, int B, int T, int K, int R, int vocab, int greedy,
-                               const float* uniforms, float inv_temp, int32_t* cand_ids, float* cand_lp,
-                               float* lse, int32_t* path_ids, int32_t* path_idx, float* score, int32_t* err,
-                               cudaStream_t s);
+                               const float* gate, int B, int T, int rows_per_seq, int first, int K, int R,
+                               int vocab, int greedy, const float* uniforms, float inv_temp, int32_t* cand_ids,
+                               float* cand_lp, float* lse, int32_t* path_ids, int32_t* path_idx, float* score,
+                               int32_t* err, cudaStream_t s);
 
 // Transition tiles + Viterbi / greedy walk, one CTA per sequence. uniforms [B, T] (nullptr: no
-// sampling) and inv_temp: draw a path at temperature 1 / inv_temp instead.
+// sampling) and inv_temp: draw a path at temperature 1 / inv_temp instead. Slot t's candidates
+// (and gate row) are row first + t of the sequence's cand_rows rows; outputs are per slot.
 cudaError_t launch_transition_walk(bool bf16, const int32_t* anchor, const int32_t* cand_ids,
                                    const float* cand_lp, const void* U, const void* V, const float* gate, int B,
-                                   int T, int K, int R, int vocab, int greedy, const float* uniforms,
-                                   float inv_temp, int32_t* path_ids, int32_t* path_idx, float* score, int32_t* err,
-                                   cudaStream_t s);
+                                   int T, int cand_rows, int first, int K, int R, int vocab, int greedy,
+                                   const float* uniforms, float inv_temp, int32_t* path_ids, int32_t* path_idx,
+                                   float* score, int32_t* err, cudaStream_t s);
 
 }  // namespace df

@@ -20,7 +20,11 @@
 // rounds them to bf16 before the MMA (one rounding of V[cur_j][r] g_t[r]; fp32 embeddings keep
 // the product in fp32).
 //
-// The fused kernel first merges the sequence's T rows (warp t % 8 takes row t): the row's
+// Slots and rows: a sequence has T slots; its candidate (or LM-head) rows are rows_per_seq
+// apart and slot t is row first + t of them (first = 1 when row 0 of each block is the
+// anchor's position). Outputs are per slot.
+//
+// The fused kernel first merges the sequence's T slot rows (warp t % 8 takes slot t): the row's
 // per-partition top-16 lists and (max, sum) pairs are staged with cp.async, lse is reduced
 // across the warp and the K best candidates are picked by the warp-wide merge; they stay in
 // shared memory for the walk (and are also written out).
@@ -383,8 +387,9 @@ template <bool kBf16>
 __global__ void __launch_bounds__(32 * kWarps)
     transition_walk_kernel(const int32_t* __restrict__ anchor, const int32_t* __restrict__ cand_ids,
                            const float* __restrict__ cand_lp, const void* __restrict__ Uv,
-                           const void* __restrict__ Vv, const float* __restrict__ gate, int T, int K, int R,
-                           int vocab, int greedy, SampleArgs sa, int32_t* __restrict__ path_ids,
+                           const void* __restrict__ Vv, const float* __restrict__ gate, int T, int cand_rows,
+                           int first, int K, int R, int vocab, int greedy, SampleArgs sa,
+                           int32_t* __restrict__ path_ids,
                            int32_t* __restrict__ path_idx, float* __restrict__ score, int32_t* err) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   SmemWalk& sw = *reinterpret_cast<SmemWalk*>(smem_raw);
@@ -395,7 +400,7 @@ __global__ void __launch_bounds__(32 * kWarps)
   for (int e = threadIdx.x; e < T * kKP; e += blockDim.x) {
     const int t = e / kKP, j = e % kKP;
     if (j < K) {
-      const size_t at = ((size_t)b * T + t) * K + j;
+      const size_t at = ((size_t)b * cand_rows + first + t) * K + j;  // slot t's candidate row
       sw.ids[t][j] = clamp_id(cand_ids[at], vocab, err, DFLASH2_DEVERR_CANDIDATE_RANGE);
       sw.lp[t][j] = cand_lp[at];
     }
@@ -403,7 +408,7 @@ __global__ void __launch_bounds__(32 * kWarps)
   __syncthreads();
   pad_candidates(sw, T, K);
   __syncthreads();
-  build_tiles<kBf16>(sw, T, R, Uv, Vv, gate ? gate + (size_t)b * T * R : nullptr, stage);
+  build_tiles<kBf16>(sw, T, R, Uv, Vv, gate ? gate + ((size_t)b * cand_rows + first) * R : nullptr, stage);
   __syncthreads();
   if ((threadIdx.x >> 5) != 0) return;
   walk_warp0(sw, b, T, K, greedy, sa, path_ids, path_idx, score);
@@ -428,7 +433,7 @@ __global__ void __launch_bounds__(32 * kWarps)
     select_walk_kernel(const float* __restrict__ part_val, const int32_t* __restrict__ part_id,
                        const float2* __restrict__ part_ms, int parts, int M, const int32_t* __restrict__ anchor,
                        const void* __restrict__ Uv, const void* __restrict__ Vv, const float* __restrict__ gate,
-                       int T, int K, int R, int vocab,
+                       int T, int rows_per_seq, int first, int K, int R, int vocab,
                        int greedy, SampleArgs sa, int32_t* __restrict__ cand_ids, float* __restrict__ cand_lp,
                        float* __restrict__ lse_out, int32_t* __restrict__ path_ids, int32_t* __restrict__ path_idx,
                        float* __restrict__ score, int32_t* err) {
@@ -468,7 +473,8 @@ __global__ void __launch_bounds__(32 * kWarps)
     float2* sms = reinterpret_cast<float2*>(si + parts * 16);
     uint8_t* head = reinterpret_cast<uint8_t*>(sms + parts);
     for (int t = warp; t < T; t += kWarps) {
-      const int row = b * T + t;
+      const int row = b * rows_per_seq + first + t;  // slot t's row of the LM-head pass
+      const int slot = b * T + t;
       // the row's lists and (max, sum) pairs in one batch of async copies
       for (int e = lane; e < parts * 4; e += 32) {
         const int p = e >> 2, q = e & 3;
@@ -493,7 +499,7 @@ __global__ void __launch_bounds__(32 * kWarps)
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
       const float lse = m + logf(s);
-      if (lane == 0 && lse_out) lse_out[row] = lse;
+      if (lane == 0 && lse_out) lse_out[slot] = lse;
       warp_merge_lists(sv, si, head, parts, K, [&](int k, int32_t id, float v) {
         const float lp = v - lse;
         // every merged id indexes U and V below: a partial that held no column would carry an
@@ -501,8 +507,8 @@ __global__ void __launch_bounds__(32 * kWarps)
         id = clamp_id(id, vocab, err, DFLASH2_DEVERR_CANDIDATE_RANGE);
         sw.ids[t][k] = id;
         sw.lp[t][k] = lp;
-        if (cand_ids) cand_ids[(size_t)row * K + k] = id;
-        if (cand_lp) cand_lp[(size_t)row * K + k] = lp;
+        if (cand_ids) cand_ids[(size_t)slot * K + k] = id;
+        if (cand_lp) cand_lp[(size_t)slot * K + k] = lp;
       });
       __syncwarp();
       if (early) {
@@ -528,7 +534,7 @@ __global__ void __launch_bounds__(32 * kWarps)
           warp == 0 ? a0 : reinterpret_cast<const __nv_bfloat16*>(region + (warp - 1) * wstride) + kKP * kRowPad;
       __nv_bfloat16* stB = reinterpret_cast<__nv_bfloat16*>(region + warp * wstride);
       if (gate) {
-        gate_rows(stB, R, gate + ((size_t)b * T + warp) * R);
+        gate_rows(stB, R, gate + ((size_t)b * rows_per_seq + first + warp) * R);
         __syncwarp();
       }
       float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -540,7 +546,7 @@ __global__ void __launch_bounds__(32 * kWarps)
     __syncthreads();
     pad_candidates(sw, T, K);
     __syncthreads();
-    build_tiles<kBf16>(sw, T, R, Uv, Vv, gate ? gate + (size_t)b * T * R : nullptr,
+    build_tiles<kBf16>(sw, T, R, Uv, Vv, gate ? gate + ((size_t)b * rows_per_seq + first) * R : nullptr,
                        reinterpret_cast<__nv_bfloat16*>(region));
     __syncthreads();
   }
@@ -559,10 +565,11 @@ size_t select_walk_smem(int parts) {
 
 cudaError_t launch_select_walk(bool bf16, const float* part_val, const int32_t* part_id, const float* part_ms,
                                int parts, int M, const int32_t* anchor, const void* U, const void* V,
-                               const float* gate, int B, int T, int K, int R, int vocab, int greedy,
-                               const float* uniforms, float inv_temp, int32_t* cand_ids, float* cand_lp,
-                               float* lse, int32_t* path_ids, int32_t* path_idx, float* score, int32_t* err,
-                               cudaStream_t s) {
+                               const float* gate, int B, int T, int rows_per_seq, int first, int K, int R,
+                               int vocab, int greedy, const float* uniforms, float inv_temp, int32_t* cand_ids,
+                               float* cand_lp, float* lse, int32_t* path_ids, int32_t* path_idx, float* score,
+                               int32_t* err, cudaStream_t s) {
+  if (first < 0 || first + T > rows_per_seq) return cudaErrorInvalidValue;
   const SampleArgs sa{uniforms, inv_temp};
   if (T > kMaxT || K > kKP) return cudaErrorInvalidValue;
   const size_t smem = select_walk_smem(parts);
@@ -584,15 +591,17 @@ cudaError_t launch_select_walk(bool bf16, const float* part_val, const int32_t* 
     static unsigned char smem_done[64];
     e = smem_opt_in(reinterpret_cast<const void*>(select_walk_kernel<true>), smem_done);
     if (e != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, select_walk_kernel<true>, part_val, part_id, ms, parts, M, anchor, U, V, gate, T, K,
-                           R, vocab, greedy, sa, cand_ids, cand_lp, lse, path_ids, path_idx, score, err);
+    e = cudaLaunchKernelEx(&cfg, select_walk_kernel<true>, part_val, part_id, ms, parts, M, anchor, U, V, gate, T,
+                           rows_per_seq, first, K, R, vocab, greedy, sa, cand_ids, cand_lp, lse, path_ids,
+                           path_idx, score, err);
     if (e != cudaSuccess) return e;
   } else {
     static unsigned char smem_done[64];
     e = smem_opt_in(reinterpret_cast<const void*>(select_walk_kernel<false>), smem_done);
     if (e != cudaSuccess) return e;
     e = cudaLaunchKernelEx(&cfg, select_walk_kernel<false>, part_val, part_id, ms, parts, M, anchor, U, V, gate, T,
-                           K, R, vocab, greedy, sa, cand_ids, cand_lp, lse, path_ids, path_idx, score, err);
+                           rows_per_seq, first, K, R, vocab, greedy, sa, cand_ids, cand_lp, lse, path_ids,
+                           path_idx, score, err);
     if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
@@ -600,9 +609,10 @@ cudaError_t launch_select_walk(bool bf16, const float* part_val, const int32_t* 
 
 cudaError_t launch_transition_walk(bool bf16, const int32_t* anchor, const int32_t* cand_ids,
                                    const float* cand_lp, const void* U, const void* V, const float* gate, int B,
-                                   int T, int K, int R, int vocab, int greedy, const float* uniforms,
-                                   float inv_temp, int32_t* path_ids, int32_t* path_idx, float* score, int32_t* err,
-                                   cudaStream_t s) {
+                                   int T, int cand_rows, int first, int K, int R, int vocab, int greedy,
+                                   const float* uniforms, float inv_temp, int32_t* path_ids, int32_t* path_idx,
+                                   float* score, int32_t* err, cudaStream_t s) {
+  if (first < 0 || first + T > cand_rows) return cudaErrorInvalidValue;
   const SampleArgs sa{uniforms, inv_temp};
   if (T > kMaxT || K > kKP) return cudaErrorInvalidValue;
   const size_t base = (sizeof(SmemWalk) + 127) & ~size_t(127);
@@ -612,14 +622,16 @@ cudaError_t launch_transition_walk(bool bf16, const int32_t* anchor, const int32
     static unsigned char smem_done[64];
     e = smem_opt_in(reinterpret_cast<const void*>(transition_walk_kernel<true>), smem_done);
     if (e != cudaSuccess) return e;
-    transition_walk_kernel<true><<<B, 32 * kWarps, smem, s>>>(anchor, cand_ids, cand_lp, U, V, gate, T, K, R,
-                                                               vocab, greedy, sa, path_ids, path_idx, score, err);
+    transition_walk_kernel<true><<<B, 32 * kWarps, smem, s>>>(anchor, cand_ids, cand_lp, U, V, gate, T, cand_rows,
+                                                               first, K, R, vocab, greedy, sa, path_ids, path_idx,
+                                                               score, err);
   } else {
     static unsigned char smem_done[64];
     e = smem_opt_in(reinterpret_cast<const void*>(transition_walk_kernel<false>), smem_done);
     if (e != cudaSuccess) return e;
-    transition_walk_kernel<false><<<B, 32 * kWarps, smem, s>>>(anchor, cand_ids, cand_lp, U, V, gate, T, K, R,
-                                                                vocab, greedy, sa, path_ids, path_idx, score, err);
+    transition_walk_kernel<false><<<B, 32 * kWarps, smem, s>>>(anchor, cand_ids, cand_lp, U, V, gate, T,
+                                                                cand_rows, first, K, R, vocab, greedy, sa, path_ids,
+                                                                path_idx, score, err);
   }
   return cudaGetLastError();
 }

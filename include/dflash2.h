@@ -63,8 +63,19 @@ enum {
   DFLASH2_CONV_TAPS_SOFTMAX = 0,      /* default: each group's 2 taps are softmax-normalised */
   DFLASH2_CONV_TAPS_RAW = 1u << 0,    /* taps used as projected, unnormalised */
   DFLASH2_WALK_VITERBI = 0,           /* default: exact best path (Viterbi) */
-  DFLASH2_WALK_GREEDY = 1u << 1       /* the pages' greedy walk: best successor at each step */
+  DFLASH2_WALK_GREEDY = 1u << 1,      /* the pages' greedy walk: best successor at each step */
+  DFLASH2_FIRST_SLOT_1 = 1u << 2      /* row 0 of each block is the anchor's own position */
 };
+
+/* Slots. By default all `block` rows of a sequence are slots and the anchor is the token
+ * before slot 0. With DFLASH2_FIRST_SLOT_1 (block >= 2), row 0 of each block is the anchor's
+ * own position (the block is 1 + the speculative tokens: "RTX 4090 ... DFlash2 vs MTP",
+ * section 4): its hidden row goes through the conv with the others, so the slots see it, and
+ * the slots are rows 1..block-1, walked from the anchor token. S = block - 1 slots then, and
+ * every per-slot argument of the walk calls (cand_ids, cand_lp, lse, gate, uniforms,
+ * path_ids, path_idx) has S slots per sequence instead of block. dflash2_conv and
+ * dflash2_select_topk work on all B*block rows either way; the tail's gate output (when
+ * requested) holds every row's gate, [B, block, R]. */
 
 /* Device error word bits (dflash2_read_device_error). */
 enum {

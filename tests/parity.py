@@ -42,7 +42,8 @@ GATE_TOL = 1e-3
 
 def shape_of(sh, greedy=False) -> df2.Shape:
     return df2.Shape.make(sh.batch, sh.block, sh.hidden, sh.vocab, sh.top_k, sh.rank, sh.layers,
-                          dtype=sh.dtype, raw_taps=(sh.taps == "raw"), greedy=greedy)
+                          dtype=sh.dtype, raw_taps=(sh.taps == "raw"), greedy=greedy,
+                          first_slot=getattr(sh, "first_slot", 0))
 
 
 def dev(a: np.ndarray) -> torch.Tensor:
@@ -71,15 +72,18 @@ def upload_inputs(inp: dict) -> dict:
 
 
 def run_tail(shape: df2.Shape, d: dict, ws=None, stream=None, gated=False) -> dict:
-    """The whole tail through dflash2_draft_tail, or dflash2_draft_tail_gated (gate rows out)."""
+    """The whole tail through dflash2_draft_tail, or dflash2_draft_tail_gated (gate rows out).
+    Per-slot outputs have S = block - first slots (first = 1 with DFLASH2_FIRST_SLOT_1); the gate
+    rows cover every row."""
     B, T, K = shape.batch, shape.block, shape.top_k
+    S = T - (1 if shape.flags & df2.FIRST_SLOT_1 else 0)
     o = {
-        "path_ids": torch.empty((B, T), dtype=torch.int32, device="cuda:0"),
-        "path_idx": torch.empty((B, T), dtype=torch.int32, device="cuda:0"),
+        "path_ids": torch.empty((B, S), dtype=torch.int32, device="cuda:0"),
+        "path_idx": torch.empty((B, S), dtype=torch.int32, device="cuda:0"),
         "score": torch.empty((B,), dtype=torch.float32, device="cuda:0"),
-        "cand_ids": torch.empty((B, T, K), dtype=torch.int32, device="cuda:0"),
-        "cand_lp": torch.empty((B, T, K), dtype=torch.float32, device="cuda:0"),
-        "lse": torch.empty((B, T), dtype=torch.float32, device="cuda:0"),
+        "cand_ids": torch.empty((B, S, K), dtype=torch.int32, device="cuda:0"),
+        "cand_lp": torch.empty((B, S, K), dtype=torch.float32, device="cuda:0"),
+        "lse": torch.empty((B, S), dtype=torch.float32, device="cuda:0"),
     }
     ws = workspace(shape) if ws is None else ws
     if gated:
@@ -125,8 +129,10 @@ def run_topk(shape: df2.Shape, rows: torch.Tensor, lm_head: torch.Tensor):
 
 
 def run_viterbi(shape: df2.Shape, anchor, cand_ids, cand_lp, U, V, gate=None):
-    """dflash2_viterbi, or dflash2_viterbi_gated when gate [B,T,R] fp32 is given."""
-    B, T = shape.batch, shape.block
+    """dflash2_viterbi, or dflash2_viterbi_gated when gate [B,S,R] fp32 is given (S slots:
+    block, or block - 1 with DFLASH2_FIRST_SLOT_1)."""
+    B = shape.batch
+    T = shape.block - (1 if shape.flags & df2.FIRST_SLOT_1 else 0)
     pid = torch.empty((B, T), dtype=torch.int32, device="cuda:0")
     pix = torch.empty((B, T), dtype=torch.int32, device="cuda:0")
     sc = torch.empty((B,), dtype=torch.float32, device="cuda:0")
@@ -244,15 +250,17 @@ def check_gate(g_gpu: np.ndarray, g_ref: np.ndarray) -> dict:
 def check_tail(shape, inp: dict, ref: dict, g: dict, seqs=None) -> dict:
     """Compare a draft_tail result with the oracle on the listed sequences, step by step (see
     the module docstring); ref is the oracle's end-to-end result for those sequences."""
-    B, T, K, H = shape.batch, shape.block, shape.top_k, shape.hidden
+    B, K, H = shape.batch, shape.top_k, shape.hidden
+    first = int(getattr(shape, "first_slot", 0))
+    T = shape.block - first  # slots per sequence
     seqs = list(range(B)) if seqs is None else list(seqs)
     assert g["device_error"] == 0, f"device error word {g['device_error']}"
     sel = np.asarray(seqs)
-    # 1. conv
+    # 1. conv (every row)
     rep = check_conv(g["z"][sel], ref["z"])
-    # 2. selection, on the GPU's own conv output
+    # 2. selection, on the GPU's own conv output (the slot rows)
     ref_g = O.select_from_z(g["z"][sel], inp, shape, seqs)
-    z_rows = ref_g["z"].reshape(-1, H)
+    z_rows = ref_g["z"][:, first:, :].reshape(-1, H)
     rows = (sel[:, None] * T + np.arange(T)[None, :]).reshape(-1)
     g_ids = g["cand_ids"].reshape(B * T, K)[rows]
     g_lp = g["cand_lp"].reshape(B * T, K)[rows]
@@ -261,7 +269,7 @@ def check_tail(shape, inp: dict, ref: dict, g: dict, seqs=None) -> dict:
     g_gate = None
     if getattr(shape, "gate", False):
         # the gate rows: H(h_t) of the GPU's own conv output (fp32 sums of bf16 products)
-        g_gate = g["gate"][sel]
+        g_gate = g["gate"][sel][:, first:]
         rep.update(check_gate(g_gate.reshape(-1, g_gate.shape[-1]), ref_g["gate"].reshape(-1, g_gate.shape[-1])))
 
     class _S:  # the subset as a shape
