@@ -282,7 +282,7 @@ dflash2_status_t run_partials(const Plan& p, const void* rows, const void* lm_he
                p.lm_cluster, w.err};
   if (gate_w) {
     // the gate rows are one more partition: the last CTA's (the vocabulary keeps the others)
-    if (!p.bf16 || !gate_out) return DFLASH2_ERR_UNSUPPORTED;
+    if (!gate_out) return DFLASH2_ERR_INVALID_ARGUMENT;
     a.parts = gated_parts(p);
     a.gate_base = (p.V + 15) / 16 * 16;
     a.gate_cols = p.R;
@@ -307,8 +307,9 @@ dflash2_status_t run_partials(const Plan& p, const void* rows, const void* lm_he
                                     gate_w ? gate_out : nullptr, s) != cudaSuccess)
       return DFLASH2_ERR_CUDA;
   } else {
-    if (df::launch_lmhead_topk_f32(static_cast<const float*>(rows), static_cast<const float*>(lm_head), a,
-                                   w.part_val, w.part_id, w.part_ms, s) != cudaSuccess)
+    if (df::launch_lmhead_topk_f32(static_cast<const float*>(rows), static_cast<const float*>(lm_head),
+                                   static_cast<const float*>(gate_w), a, w.part_val, w.part_id, w.part_ms,
+                                   gate_w ? gate_out : nullptr, s) != cudaSuccess)
       return DFLASH2_ERR_CUDA;
   }
   return DFLASH2_OK;
@@ -415,7 +416,6 @@ dflash2_status_t dflash2_select_topk_gated(const dflash2_shape_t* shape, const v
   if (st != DFLASH2_OK) return st;
   if (!rows || !lm_head || !cand_ids || !cand_lp || (gate_w && !gate)) return DFLASH2_ERR_INVALID_ARGUMENT;
   if (!aligned16(rows) || !aligned16(lm_head) || (gate_w && !aligned16(gate_w))) return DFLASH2_ERR_INVALID_ARGUMENT;
-  if (gate_w && !p.bf16) return DFLASH2_ERR_UNSUPPORTED;
   Ws w;
   if ((st = check_ws(p, ws, ws_bytes, w)) != DFLASH2_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -529,7 +529,6 @@ dflash2_status_t dflash2_draft_tail_sampled(const dflash2_shape_t* shape, const 
     return DFLASH2_ERR_INVALID_ARGUMENT;
   if (gate && !aligned16(gate)) return DFLASH2_ERR_INVALID_ARGUMENT;
   if (uniforms && !(temperature > 0.f && temperature < 1e30f)) return DFLASH2_ERR_INVALID_ARGUMENT;
-  if (gate_w && !p.bf16) return DFLASH2_ERR_UNSUPPORTED;
   Ws w;
   if ((st = check_ws(p, ws, ws_bytes, w)) != DFLASH2_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

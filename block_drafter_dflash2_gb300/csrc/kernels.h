@@ -62,8 +62,9 @@ cudaError_t launch_conv_splitk(const ConvSplitPlan& pl, const CUtensorMap* maps,
 // fp32 instantiations (small sizes).
 cudaError_t launch_conv_layer_f32(const float* x, const float* w, float* y, int M, int H, int T, int raw,
                                   cudaStream_t s);
-cudaError_t launch_lmhead_topk_f32(const float* z, const float* w, const TcGemmArgs& args, float* part_val,
-                                   int32_t* part_id, float* part_ms, cudaStream_t s);
+cudaError_t launch_lmhead_topk_f32(const float* z, const float* w, const float* gate_w, const TcGemmArgs& args,
+                                   float* part_val, int32_t* part_id, float* part_ms, float* gate_out,
+                                   cudaStream_t s);
 
 // Merge of the per-partition top-16 lists and (max, sum) pairs -> top-K, log-probs, lse.
 cudaError_t launch_topk_merge(const float* part_val, const int32_t* part_id, const float* part_ms, int parts,

@@ -57,13 +57,16 @@ __global__ void __launch_bounds__(256) conv_layer_f32_kernel(const float* __rest
 constexpr int kTileCols = 128;
 constexpr int kMaxRows = 64;
 
+// gw: the context gate's weights [gate_cols, H] (the gate partition's rows), or nullptr.
 __global__ void __launch_bounds__(128) lmhead_topk_f32_kernel(const float* __restrict__ z,
-                                                               const float* __restrict__ w, TcGemmArgs args,
+                                                               const float* __restrict__ w,
+                                                               const float* __restrict__ gw, TcGemmArgs args,
                                                                EpiTopK::Params ep) {
   __shared__ float tile[kMaxRows][kTileCols + 1];
   const int part = blockIdx.x;
   if (part >= args.parts) return;
   const TileRange tr = tile_range(args, part);
+  const bool gate_part = is_gate_part(args, part);
   const int t = threadIdx.x;
   const int M = args.M, H = args.K;
   EpiTopK::State st;
@@ -74,7 +77,7 @@ __global__ void __launch_bounds__(128) lmhead_topk_f32_kernel(const float* __res
     for (int r = 0; r < M; ++r) {
       float s = 0.f;
       if (col_ok) {
-        const float* wr = w + (size_t)col * H;
+        const float* wr = gate_part ? gw + (size_t)(col - args.gate_base) * H : w + (size_t)col * H;
         const float* zr = z + (size_t)r * H;
         for (int h = 0; h < H; ++h) s = fmaf(zr[h], wr[h], s);
       }
@@ -102,11 +105,15 @@ cudaError_t launch_conv_layer_f32(const float* x, const float* w, float* y, int 
   return cudaGetLastError();
 }
 
-cudaError_t launch_lmhead_topk_f32(const float* z, const float* w, const TcGemmArgs& args, float* part_val,
-                                   int32_t* part_id, float* part_ms, cudaStream_t s) {
+cudaError_t launch_lmhead_topk_f32(const float* z, const float* w, const float* gate_w, const TcGemmArgs& args,
+                                   float* part_val, int32_t* part_id, float* part_ms, float* gate_out,
+                                   cudaStream_t s) {
   if (args.M > kMaxRows) return cudaErrorInvalidValue;
-  EpiTopK::Params ep{part_val, part_id, part_ms, args.M, args.n_total, nullptr, 0, 0};  // no gate columns
-  lmhead_topk_f32_kernel<<<args.parts, 128, 0, s>>>(z, w, args, ep);
+  if (args.gate_cols > 0 && (gate_w == nullptr || gate_out == nullptr || args.parts < 2 ||
+                             args.gate_base < args.n_total))
+    return cudaErrorInvalidValue;
+  EpiTopK::Params ep{part_val, part_id, part_ms, args.M, args.n_total, gate_out, args.gate_base, args.gate_cols};
+  lmhead_topk_f32_kernel<<<args.parts, 128, 0, s>>>(z, w, gate_w, args, ep);
   return cudaGetLastError();
 }
 

@@ -355,8 +355,10 @@ struct EpiTopK {
       if (p.gate_cols > 0) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
+          // only this partition's columns (a chunk may run past the partition's end)
           const int c = col0 + i - p.gate_base;
-          if (i < ncols && c >= 0 && c < p.gate_cols) p.gate_out[(size_t)row * p.gate_cols + c] = v[i];
+          if (i < ncols && col0 + i < col_end && c >= 0 && c < p.gate_cols)
+            p.gate_out[(size_t)row * p.gate_cols + c] = v[i];
         }
       }
       col_end = min(col_end, p.vocab);

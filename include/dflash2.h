@@ -135,9 +135,9 @@ dflash2_status_t dflash2_select_topk(const dflash2_shape_t* shape, const void* r
  * and the gated transition is tau_t(i, j) = sum_r U[prev_i, r] * gate[slot t, r] * V[cur_j, r]
  * (the gate of the current slot t; for t = 0 the anchor is the previous token).
  * The gate is contracted in the LM-head pass itself (its R rows are appended to the head's
- * columns), so it costs no extra pass over the rows. bf16 only; dtype FP32 returns
- * DFLASH2_ERR_UNSUPPORTED. In the walk, V[cur_j, r] * gate[r] is rounded to bf16 once before
- * the fp32-accumulated product with U (fp32 embeddings keep it in fp32).
+ * columns), so it costs no extra pass over the rows. gate_w has the call's dtype. In the walk,
+ * V[cur_j, r] * gate[r] is rounded to bf16 once before the fp32-accumulated product with U
+ * (fp32 embeddings keep it in fp32).
  *
  * dflash2_select_topk_gated: dflash2_select_topk plus gate [M, R] fp32 out (gate_w non-NULL;
  * gate_w NULL is dflash2_select_topk, gate ignored). */

@@ -125,3 +125,19 @@ def test_viterbi_gate_of_ones_is_ungated_bitwise():
     p1 = P.run_viterbi(P.shape_of(sh), *args, gate=P.dev(np.ones((B, T, R), np.float32)))
     for a, b in zip(p0[:3], p1[:3]):
         assert np.array_equal(a, b)
+
+
+def test_tiny_fp32_workload_gated():
+    # dtype fp32: the gate partition of the SIMT LM-head kernel, the fp32 gated tiles
+    rc = synth.recipe(1)
+    sh = rc.shape
+    sh.gate = True
+    inp = synth.make_inputs(rc)
+    ref = O.draft_tail(inp, sh)
+    g = P.run_tail(P.shape_of(sh), P.upload_inputs(inp), gated=True)
+    rep = P.check_tail(sh, inp, ref, g)
+    assert rep["gate_max_abs_err"] < 1e-4
+    # the walk is the brute-force best path over the GPU's candidates and gate rows (4^4 paths)
+    tau = O.transitions(inp["anchor"], g["cand_ids"], inp["U"], inp["V"], g["gate"])
+    bp, _ = O.brute_force_best(g["cand_lp"], tau)
+    assert np.array_equal(bp, g["path_idx"])
