@@ -25,15 +25,11 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& a_tail, const C
   cfg.blockDim = dim3(kGemmThreads);
   cfg.dynamicSmemBytes = kGemmSmemBytes;
   cfg.stream = s;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = args.n_rc == 1 ? 1 : 0;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = args.cluster;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = args.cluster > 1 ? 2 : 1;
+  cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<Epi>, a, a_tail, b128, b16, g128, g16, args, ep);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -45,7 +41,7 @@ cudaError_t launch_lmhead_topk_bf16(const CUtensorMap& a, const CUtensorMap& a_t
                                     const TcGemmArgs& args, int vocab, float* part_val, int32_t* part_id,
                                     float* part_ms, float* gate_out, cudaStream_t s) {
   if (args.gate_cols > 0 && (args.gate_base < vocab || args.gate_base % 16 != 0 || gate_out == nullptr ||
-                             args.n_total != vocab || args.parts < 2 || args.cluster != 1))
+                             args.n_total != vocab || args.parts < 2))
     return cudaErrorInvalidValue;
   EpiTopK::Params ep{part_val, part_id, part_ms, args.M, vocab, gate_out, args.gate_base, args.gate_cols};
   return launch_gemm<EpiTopK>(a, a_tail, b128, b16, g128, g16, args, ep, s);

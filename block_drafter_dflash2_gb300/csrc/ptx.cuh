@@ -105,34 +105,6 @@ DF_DEV void tma_load_2d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, i
       : "memory");
 }
 
-// Same load, written to the same shared-memory offset of every CTA in `mask` (this CTA's
-// cluster), each destination's mbarrier at `bar`'s offset receiving the bytes it got.
-// The 16-bit CTA mask enters the asm as a 32-bit register and is narrowed inside it: handed
-// over as a 16-bit operand, it arrived with stray upper bits in some register allocations and
-// the copies never reached their CTAs.
-DF_DEV void tma_load_2d_mc(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int32_t c0, int32_t c1,
-                           uint16_t mask, uint64_t policy) {
-  asm volatile(
-      "{\n\t.reg .b16 m;\n\tcvt.u16.u32 m, %5;\n\t"
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], m, %6;\n\t}" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"((uint32_t)mask), "l"(policy)
-      : "memory");
-}
-
-// ---------------------------------------------------------------- clusters
-
-DF_DEV uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// All threads of all CTAs of the cluster (hardware barrier).
-DF_DEV void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 // ---------------------------------------------------------------- tcgen05
 
 DF_DEV void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
@@ -165,18 +137,6 @@ DF_DEV void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_u32(bar))
                : "memory");
-}
-
-// Arrive once on the mbarrier at `bar`'s offset in every CTA of `mask`, when every MMA issued
-// so far by this thread has completed.
-// (The mask is narrowed inside the asm, as for tma_load_2d_mc.)
-DF_DEV void umma_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "{\n\t.reg .b16 m;\n\tcvt.u16.u32 m, %1;\n\t"
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], m;\n\t}" ::"r"(
-          smem_u32(bar)),
-      "r"((uint32_t)mask)
-      : "memory");
 }
 
 // Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, shape M x N.

@@ -81,11 +81,9 @@ DF_DEV StageGeom stage_geom(const TcGemmArgs& a, int rc, const TileRange& tr) {
   StageGeom g;
   const int rows = (rc == a.n_rc - 1) ? a.a_tail_rows : kBM;
   g.a_bytes = (uint32_t)rows * kBK * 2;
-  // CTAs of a cluster write B tiles into each other's rings: one layout for all of them
-  const uint32_t a_region = a.cluster > 1 ? (uint32_t)kBM * kBK * 2 : g.a_bytes;
   const int nmax = min(a.tile_units, tr.u1 - tr.u0) * 16;
-  g.b_off = a_region;
-  g.stride = (a_region + (uint32_t)nmax * kBK * 2 + 1023u) & ~1023u;
+  g.b_off = g.a_bytes;
+  g.stride = (g.a_bytes + (uint32_t)nmax * kBK * 2 + 1023u) & ~1023u;
   g.stages = min(kMaxStages, (int)(kRingBytes / g.stride));
   return g;
 }
@@ -119,14 +117,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int TU = args.tile_units;                   // tile width in 16-column units (8 or 16)
   const uint32_t tmem_cols = (uint32_t)(2 * TU * 16);  // two accumulators: 256 or 512 columns
 
-  const int CL = args.cluster;
-  const uint16_t cl_mask = (uint16_t)((1u << CL) - 1u);
-  const int crank = CL > 1 ? (int)cluster_ctarank() : 0;
   pdl_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < sg.stages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], CL);  // released by the MMA warp of every CTA reading the stage
+      mbar_init(&empty[s], 1);  // released by the MMA warp's commit
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -151,7 +146,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (CL > 1) cluster_sync();  // peers' barriers are initialised before anything lands in them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -187,28 +181,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           uint8_t* sb = sa + sg.b_off;
           mbar_arrive_expect_tx(&full[stage], bytes);
           tma_load_2d(sa, ma, &full[stage], kb * kBK, rc * kBM, pol_a);
-          if (CL == 1) {
-            if (nu % 8 == 0) {
-              for (int j = 0; j < nu / 8; ++j)
-                tma_load_2d(sb + j * 128 * kBK * 2, mb128, &full[stage], kb * kBK, n0 - row0 + 128 * j, pol_b);
-            } else {
-              for (int j = 0; j < nu; ++j)
-                tma_load_2d(sb + j * 16 * kBK * 2, mb16, &full[stage], kb * kBK, n0 - row0 + 16 * j, pol_b);
-            }
+          if (nu % 8 == 0) {
+            for (int j = 0; j < nu / 8; ++j)
+              tma_load_2d(sb + j * 128 * kBK * 2, mb128, &full[stage], kb * kBK, n0 - row0 + 128 * j, pol_b);
           } else {
-            // this CTA's share of the B tile, multicast into every CTA of the cluster
-            const int j0 = crank * nu / CL, j1 = (crank + 1) * nu / CL;
-            for (int j = j0; j < j1;) {
-              if ((j1 - j) >= 8 && (j % 8) == 0) {
-                tma_load_2d_mc(sb + j * 16 * kBK * 2, &map_b128, &full[stage], kb * kBK, n0 + 16 * j, cl_mask,
-                               pol_b);
-                j += 8;
-              } else {
-                tma_load_2d_mc(sb + j * 16 * kBK * 2, &map_b16, &full[stage], kb * kBK, n0 + 16 * j, cl_mask,
-                               pol_b);
-                j += 1;
-              }
-            }
+            for (int j = 0; j < nu; ++j)
+              tma_load_2d(sb + j * 16 * kBK * 2, mb16, &full[stage], kb * kBK, n0 - row0 + 16 * j, pol_b);
           }
           issued |= 1ull << stage;
           issued_phase = (issued_phase & ~(1ull << stage)) | ((uint64_t)phase << stage);
@@ -252,8 +230,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)  // 16 bf16 = 32 B per MMA along K: +2 in 16-B units
             umma_bf16(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
-          if (CL == 1) umma_commit(&empty[stage]);
-          else umma_commit_mc(&empty[stage], cl_mask);  // the stage is free once every CTA read it
+          umma_commit(&empty[stage]);
           if (++stage == sg.stages) {
             stage = 0;
             phase ^= 1u;
@@ -298,7 +275,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, tmem_cols);
   }
-  if (CL > 1) cluster_sync();  // no CTA leaves while a peer may still write into it
 }
 
 // ---------------------------------------------------------------------------
