@@ -29,6 +29,7 @@ CONV_TAPS_RAW = 1 << 0
 WALK_VITERBI = 0
 WALK_GREEDY = 1 << 1
 FIRST_SLOT_1 = 1 << 2  # row 0 of each block is the anchor's position; slots are rows 1..block-1
+SCORE_LOGITS = 1 << 3  # whole-tail calls: the walk's score on raw logits (log-softmax score + sum of lse)
 
 DEVERR_ANCHOR_RANGE = 1 << 0
 DEVERR_CANDIDATE_RANGE = 1 << 1
@@ -54,9 +55,9 @@ class Shape(ctypes.Structure):
     @classmethod
     def make(cls, batch, block, hidden, vocab, top_k, rank, conv_layers, dtype="bf16",
              conv_group_size=16, conv_kernel_size=2, raw_taps=False, greedy=False,
-             first_slot=0) -> "Shape":
+             first_slot=0, score_logits=False) -> "Shape":
         flags = (CONV_TAPS_RAW if raw_taps else 0) | (WALK_GREEDY if greedy else 0) | \
-            (FIRST_SLOT_1 if first_slot else 0)
+            (FIRST_SLOT_1 if first_slot else 0) | (SCORE_LOGITS if score_logits else 0)
         dt = {"bf16": BF16, "f32": FP32, BF16: BF16, FP32: FP32}[dtype]
         return cls(batch, block, hidden, vocab, top_k, rank, conv_group_size, conv_kernel_size,
                    conv_layers, dt, flags)

@@ -104,7 +104,7 @@ struct Plan {
   df::ConvChainPlan chain_plan;
   bool split;                // all conv layers in one cooperative launch, split-K (larger M)
   df::ConvSplitPlan split_plan;
-  bool raw, greedy;
+  bool raw, greedy, score_logits;
   int first;  // 1: row 0 of each block is the anchor's position (DFLASH2_FIRST_SLOT_1), else 0
   int S;      // slots per sequence: T - first
 };
@@ -115,7 +115,8 @@ dflash2_status_t make_plan(const dflash2_shape_t* s, Plan& p) {
       s->conv_layers < 0)
     return DFLASH2_ERR_INVALID_ARGUMENT;
   if (s->dtype != DFLASH2_BF16 && s->dtype != DFLASH2_FP32) return DFLASH2_ERR_INVALID_ARGUMENT;
-  if (s->flags & ~(uint32_t)(DFLASH2_CONV_TAPS_RAW | DFLASH2_WALK_GREEDY | DFLASH2_FIRST_SLOT_1))
+  if (s->flags & ~(uint32_t)(DFLASH2_CONV_TAPS_RAW | DFLASH2_WALK_GREEDY | DFLASH2_FIRST_SLOT_1 |
+                             DFLASH2_SCORE_LOGITS))
     return DFLASH2_ERR_INVALID_ARGUMENT;
   if ((s->flags & DFLASH2_FIRST_SLOT_1) && s->block < 2) return DFLASH2_ERR_INVALID_ARGUMENT;
   if (s->hidden % 64 != 0 || s->conv_group_size != 16 || s->conv_kernel_size != 2 || s->top_k > 16 ||
@@ -136,6 +137,7 @@ dflash2_status_t make_plan(const dflash2_shape_t* s, Plan& p) {
   p.esz = p.bf16 ? 2 : 4;
   p.raw = (s->flags & DFLASH2_CONV_TAPS_RAW) != 0;
   p.greedy = (s->flags & DFLASH2_WALK_GREEDY) != 0;
+  p.score_logits = (s->flags & DFLASH2_SCORE_LOGITS) != 0;
   p.first = (s->flags & DFLASH2_FIRST_SLOT_1) ? 1 : 0;
   p.S = p.T - p.first;
   if (!p.bf16 && (p.M > 64 || p.H > 4096)) return DFLASH2_ERR_UNSUPPORTED;
@@ -315,16 +317,21 @@ dflash2_status_t run_merge(const Plan& p, int32_t* ids, float* lp, float* lse, c
                                            p.K, ids, lp, lse ? lse : w.lse, s));
 }
 
-// The walk over p.S slots. ids / lp / gate hold cand_rows rows per sequence and slot t is row
-// first + t (the caller's per-slot arrays: cand_rows = S, first = 0). uniforms [B, S]
+// Walk flags of the kernels for this plan.
+int walk_flags(const Plan& p) {
+  return (p.greedy ? df::kWalkFlagGreedy : 0) | (p.score_logits ? df::kWalkFlagScoreLogits : 0);
+}
+
+// The walk over p.S slots. ids / lp / gate / lse_rows hold cand_rows rows per sequence and slot t
+// is row first + t (the caller's per-slot arrays: cand_rows = S, first = 0). uniforms [B, S]
 // (nullptr: the Viterbi / greedy walk) and inv_temp: draw a path instead.
 dflash2_status_t run_walk(const Plan& p, const int32_t* anchor, const int32_t* ids, const float* lp,
-                          const void* U, const void* V, const float* gate, int32_t* path_ids, int32_t* path_idx,
-                          float* score, const Ws& w, cudaStream_t s, const float* uniforms, float inv_temp,
-                          int cand_rows, int first) {
-  return cuda_status(df::launch_transition_walk(p.bf16, anchor, ids, lp, U, V, gate, p.B, p.S, cand_rows, first, p.K,
-                                                p.R, p.V, p.greedy ? 1 : 0, uniforms, inv_temp, path_ids, path_idx,
-                                                score, w.err, s));
+                          const void* U, const void* V, const float* gate, const float* lse_rows, int32_t* path_ids,
+                          int32_t* path_idx, float* score, const Ws& w, cudaStream_t s, const float* uniforms,
+                          float inv_temp, int cand_rows, int first) {
+  return cuda_status(df::launch_transition_walk(p.bf16, anchor, ids, lp, U, V, gate, lse_rows, p.B, p.S, cand_rows,
+                                                first, p.K, p.R, p.V, walk_flags(p), uniforms, inv_temp, path_ids,
+                                                path_idx, score, w.err, s));
 }
 
 // ---- scratch for dflash2_select_topk_noalloc: a fixed device array instead of a caller
@@ -483,9 +490,11 @@ dflash2_status_t dflash2_sample_walk(const dflash2_shape_t* shape, const int32_t
     return DFLASH2_ERR_INVALID_ARGUMENT;
   if (!aligned16(U) || !aligned16(V) || (gate && !aligned16(gate))) return DFLASH2_ERR_INVALID_ARGUMENT;
   if (uniforms && !(temperature > 0.f && temperature < 1e30f)) return DFLASH2_ERR_INVALID_ARGUMENT;
+  // the score on raw logits needs each slot's lse, which only the whole-tail calls have
+  if (p.score_logits) return DFLASH2_ERR_UNSUPPORTED;
   Ws w;
   if ((st = check_ws(p, ws, ws_bytes, w)) != DFLASH2_OK) return st;
-  return run_walk(p, anchor, cand_ids, cand_lp, U, V, gate, path_ids, path_idx, score, w,
+  return run_walk(p, anchor, cand_ids, cand_lp, U, V, gate, nullptr, path_ids, path_idx, score, w,
                   static_cast<cudaStream_t>(stream), uniforms, uniforms ? 1.f / temperature : 0.f, p.S, 0);
 }
 
@@ -541,13 +550,13 @@ dflash2_status_t dflash2_draft_tail_sampled(const dflash2_shape_t* shape, const 
   const int parts = gate_w ? gated_parts(p) : p.lm_parts;
   if (df::select_walk_smem(parts) <= 227 * 1024)  // merge fused with the walk
     return cuda_status(df::launch_select_walk(p.bf16, w.part_val, w.part_id, w.part_ms, parts, p.M, anchor, U,
-                                              V, g, p.B, p.S, p.T, p.first, p.K, p.R, p.V, p.greedy ? 1 : 0,
+                                              V, g, p.B, p.S, p.T, p.first, p.K, p.R, p.V, walk_flags(p),
                                               uniforms, inv_temp, cand_ids, cand_lp, lse, path_ids, path_idx, score,
                                               w.err, s));
   // merge every row into the workspace, walk the slot rows, and copy the slot rows out
   if ((st = run_merge(p, w.cand_ids, w.cand_lp, w.lse, w, s, parts)) != DFLASH2_OK) return st;
-  if ((st = run_walk(p, anchor, w.cand_ids, w.cand_lp, U, V, g, path_ids, path_idx, score, w, s, uniforms, inv_temp,
-                     p.T, p.first)) != DFLASH2_OK)
+  if ((st = run_walk(p, anchor, w.cand_ids, w.cand_lp, U, V, g, w.lse, path_ids, path_idx, score, w, s, uniforms,
+                     inv_temp, p.T, p.first)) != DFLASH2_OK)
     return st;
   const size_t k4 = (size_t)p.K * 4;
   if (cand_ids && cudaMemcpy2DAsync(cand_ids, p.S * k4, w.cand_ids + (size_t)p.first * p.K, p.T * k4, p.S * k4, p.B,

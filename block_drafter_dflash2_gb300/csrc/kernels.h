@@ -76,19 +76,25 @@ cudaError_t launch_topk_merge(const float* part_val, const int32_t* part_id, con
 size_t select_walk_smem(int parts);
 // T slots per sequence at rows first .. first+T-1 of the sequence's rows_per_seq LM-head rows
 // (per-slot outputs); gate: [B*rows_per_seq, R] fp32 context gate of every row, or nullptr.
+// walk_flags: kWalkFlagGreedy (the greedy walk; with uniforms, per-step draws along it) |
+// kWalkFlagScoreLogits (the Viterbi / greedy score on raw logits: plus the slots' lse).
+constexpr int kWalkFlagGreedy = 1;
+constexpr int kWalkFlagScoreLogits = 2;
 cudaError_t launch_select_walk(bool bf16, const float* part_val, const int32_t* part_id, const float* part_ms,
                                int parts, int M, const int32_t* anchor, const void* U, const void* V,
                                const float* gate, int B, int T, int rows_per_seq, int first, int K, int R,
-                               int vocab, int greedy, const float* uniforms, float inv_temp, int32_t* cand_ids,
+                               int vocab, int walk_flags, const float* uniforms, float inv_temp, int32_t* cand_ids,
                                float* cand_lp, float* lse, int32_t* path_ids, int32_t* path_idx, float* score,
                                int32_t* err, cudaStream_t s);
 
 // Transition tiles + Viterbi / greedy walk, one CTA per sequence. uniforms [B, T] (nullptr: no
 // sampling) and inv_temp: draw a path at temperature 1 / inv_temp instead. Slot t's candidates
-// (and gate row) are row first + t of the sequence's cand_rows rows; outputs are per slot.
+// (and gate row, and lse_rows entry) are row first + t of the sequence's cand_rows rows; outputs
+// are per slot. lse_rows (nullable) is read only with kWalkFlagScoreLogits.
 cudaError_t launch_transition_walk(bool bf16, const int32_t* anchor, const int32_t* cand_ids,
-                                   const float* cand_lp, const void* U, const void* V, const float* gate, int B,
-                                   int T, int cand_rows, int first, int K, int R, int vocab, int greedy,
+                                   const float* cand_lp, const void* U, const void* V, const float* gate,
+                                   const float* lse_rows, int B, int T, int cand_rows, int first, int K, int R,
+                                   int vocab, int walk_flags,
                                    const float* uniforms, float inv_temp, int32_t* path_ids, int32_t* path_idx,
                                    float* score, int32_t* err, cudaStream_t s);
 

@@ -13,12 +13,17 @@
 //
 // Sampling (optional, temperature > 0): instead of the best path, warp 0 draws one from
 // P(path) ~ exp(score / temperature) by forward filtering (log-sum-exp over the previous
-// candidates) and backward inverse-CDF draws on the caller's uniforms.
+// candidates) and backward inverse-CDF draws on the caller's uniforms; or, with the greedy walk,
+// draws each step from the softmax of that step's scores given the previous draw.
 //
 // Context gate (optional): tau_t(i, j) = sum_r U[prev_i][r] g_t[r] V[cur_j][r] with g_t the gate
-// of slot t (fp32, [B*T, R]). The warp that builds tile t scales its staged V rows by g_t and
-// rounds them to bf16 before the MMA (one rounding of V[cur_j][r] g_t[r]; fp32 embeddings keep
-// the product in fp32).
+// of slot t (fp32, [B*T, R]). The warp that builds tile t forms V[cur_j][r] g_t[r] in fp32 and
+// splits it into two bf16 parts, hi = bf16(v g) and lo = bf16(v g - hi) (together within about
+// 2^-17 of the fp32 product), and contracts U with both (fp32 accumulation); fp32 embeddings keep
+// the product in fp32.
+//
+// Score on the raw logits (optional, whole-tail calls): the Viterbi / greedy score is reported
+// as sum_t logit_t(j_t) + transitions, i.e. the log-softmax score plus the slots' lse.
 //
 // Slots and rows: a sequence has T slots; its candidate (or LM-head) rows are rows_per_seq
 // apart and slot t is row first + t of them (first = 1 when row 0 of each block is the
@@ -50,6 +55,7 @@ struct SmemWalk {
   float lp[kMaxT][kKP];
   float tau[kMaxT][kKP][kKP];
   float alpha[kMaxT][kKP];  // sampling: forward log-weights
+  float lse[kMaxT];         // each slot's lse (for the score on raw logits)
   int8_t bp[kMaxT][kKP];
   int32_t anchor;
 };
@@ -116,25 +122,55 @@ __device__ __forceinline__ void store_tau(const float (&acc)[2][4], float (&tau)
   }
 }
 
-// Multiplies the 16 staged rows (cols columns each, from column c0 of the embedding) by the
-// gate g[c0 ..], rounding to bf16; one warp, after the rows have landed.
-__device__ __forceinline__ void gate_rows(__nv_bfloat16* st, int cols, const float* __restrict__ g) {
+// Gated 16 x 16 products: acc += stA * (stB (.) g)^T over rc columns (g: the gate from the first
+// staged column). Per 64-column chunk each lane forms V g in fp32 for its pieces and splits it
+// into hi = bf16(V g) and lo = bf16(V g - hi); hi is written over the staged V rows and
+// contracted, then lo, so no extra shared memory is needed. The staged V rows are consumed.
+__device__ __forceinline__ void tile_mma_gated(const __nv_bfloat16* stA, __nv_bfloat16* stB, int rc,
+                                               const float* __restrict__ g, float (&acc)[2][4]) {
   const int lane = threadIdx.x & 31;
-  const int vec_per_row = cols / 8;
-  for (int v = lane; v < kKP * vec_per_row; v += 32) {
-    const int row = v / vec_per_row, cv = v % vec_per_row;
-    uint4* p = reinterpret_cast<uint4*>(st + row * kRowPad + cv * 8);
-    const float4 g0 = __ldg(reinterpret_cast<const float4*>(g + cv * 8));
-    const float4 g1 = __ldg(reinterpret_cast<const float4*>(g + cv * 8 + 4));
-    uint4 x = *p;
-    __nv_bfloat162* x2 = reinterpret_cast<__nv_bfloat162*>(&x);
-    const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+  for (int c0 = 0; c0 < rc; c0 += 64) {
+    const int cw = min(64, rc - c0);  // a multiple of 16
+    const int vpr = cw / 8;           // 16-byte pieces per row in this chunk
+    uint4 lo[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float2 f = __bfloat1622float2(x2[k]);
-      x2[k] = __floats2bfloat162_rn(f.x * gg[2 * k], f.y * gg[2 * k + 1]);
+    for (int i = 0; i < 4; ++i) {
+      const int v = lane + 32 * i;
+      if (v < kKP * vpr) {
+        const int row = v / vpr, cv = v % vpr;
+        uint4* p = reinterpret_cast<uint4*>(stB + row * kRowPad + c0 + cv * 8);
+        const float4 g0 = __ldg(reinterpret_cast<const float4*>(g + c0 + cv * 8));
+        const float4 g1 = __ldg(reinterpret_cast<const float4*>(g + c0 + cv * 8 + 4));
+        const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+        uint4 x = *p;
+        __nv_bfloat162* x2 = reinterpret_cast<__nv_bfloat162*>(&x);
+        __nv_bfloat162* l2 = reinterpret_cast<__nv_bfloat162*>(&lo[i]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 f = __bfloat1622float2(x2[k]);
+          const float p0 = f.x * gg[2 * k], p1 = f.y * gg[2 * k + 1];
+          const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+          const float2 hf = __bfloat1622float2(h);
+          l2[k] = __floats2bfloat162_rn(p0 - hf.x, p1 - hf.y);
+          x2[k] = h;
+        }
+        *p = x;
+      }
     }
-    *p = x;
+    __syncwarp();
+    tile_mma(stA + c0, stB + c0, cw, acc);
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int v = lane + 32 * i;
+      if (v < kKP * vpr) {
+        const int row = v / vpr, cv = v % vpr;
+        *reinterpret_cast<uint4*>(stB + row * kRowPad + c0 + cv * 8) = lo[i];
+      }
+    }
+    __syncwarp();
+    tile_mma(stA + c0, stB + c0, cw, acc);
+    __syncwarp();
   }
 }
 
@@ -169,11 +205,8 @@ __device__ void tile_bf16(const __nv_bfloat16* __restrict__ U, const __nv_bfloat
     cp_async_commit();
     cp_async_wait_all();
     __syncwarp();
-    if (g) {
-      gate_rows(stB, rc, g + r0);
-      __syncwarp();
-    }
-    tile_mma(stA, stB, rc, acc);
+    if (g) tile_mma_gated(stA, stB, rc, g + r0, acc);
+    else tile_mma(stA, stB, rc, acc);
   }
   store_tau(acc, tau);
 }
@@ -302,15 +335,47 @@ __device__ void sample_warp0(SmemWalk& sw, int b, int T, int K, const SampleArgs
   if (lane == 0) score[b] = lp_sum;
 }
 
+// Per-step sampling along the greedy walk on warp 0: j_0 ~ softmax_j ((lp_0(j) + tau_0(0, j)) / T),
+// j_t ~ softmax_j ((lp_t(j) + tau_t(j_{t-1}, j)) / T), each by inverse CDF on u[b, t]; score[b]
+// receives the log-probability of the drawn path, sum_t log p_t(j_t).
+__device__ void greedy_sample_warp0(SmemWalk& sw, int b, int T, int K, const SampleArgs& sa,
+                                    int32_t* __restrict__ path_ids, int32_t* __restrict__ path_idx,
+                                    float* __restrict__ score) {
+  const int lane = threadIdx.x & 31;
+  const bool live = lane < K;
+  const float* u = sa.u + (size_t)b * T;
+  float lp_sum = 0.f, lpk;
+  int pj = 0;
+  for (int t = 0; t < T; ++t) {
+    const float lw = live ? (sw.lp[t][lane] + sw.tau[t][pj][lane]) * sa.inv_temp : -INFINITY;
+    pj = draw_index(lw, K, u[t], lpk);
+    lp_sum += lpk;
+    if (lane == 0) {
+      path_idx[(size_t)b * T + t] = pj;
+      path_ids[(size_t)b * T + t] = sw.ids[t][pj];
+    }
+  }
+  if (lane == 0) score[b] = lp_sum;
+}
+
+// Sum of the slots' lse, added to a Viterbi / greedy score reported on the raw logits.
+__device__ __forceinline__ float lse_sum(const SmemWalk& sw, int T) {
+  float s = 0.f;
+  for (int t = 0; t < T; ++t) s += sw.lse[t];
+  return s;
+}
+
 // The walk for sequence b on warp 0 (the other warps return before calling it).
-__device__ void walk_warp0(SmemWalk& sw, int b, int T, int K, int greedy, const SampleArgs& sa,
+__device__ void walk_warp0(SmemWalk& sw, int b, int T, int K, int flags, const SampleArgs& sa,
                            int32_t* __restrict__ path_ids, int32_t* __restrict__ path_idx,
                            float* __restrict__ score) {
   const int lane = threadIdx.x & 31;
   const int j = lane;
   const bool live = j < K;
+  const bool greedy = (flags & kWalkFlagGreedy) != 0;
   if (sa.u) {
-    sample_warp0(sw, b, T, K, sa, path_ids, path_idx, score);
+    if (greedy) greedy_sample_warp0(sw, b, T, K, sa, path_ids, path_idx, score);
+    else sample_warp0(sw, b, T, K, sa, path_ids, path_idx, score);
   } else if (!greedy) {
     // Viterbi in fp32: delta_0 = lp_0 + tau_0(0, j); delta_t = lp_t + max_i (delta_{t-1}(i) + tau_t(i, j)).
     // delta(i) is read back from shared memory by every lane (a broadcast), so the inner
@@ -355,7 +420,7 @@ __device__ void walk_warp0(SmemWalk& sw, int b, int T, int K, int greedy, const 
         path_ids[(size_t)b * T + t] = sw.ids[t][cj];
         if (t > 0) cj = sw.bp[t][cj];
       }
-      score[b] = bv;
+      score[b] = (flags & kWalkFlagScoreLogits) ? bv + lse_sum(sw, T) : bv;
     }
   } else {
     // Greedy: j_t = argmax_j (lp_t(j) + tau_t(j_{t-1}, j)); the score follows the Viterbi
@@ -378,7 +443,7 @@ __device__ void walk_warp0(SmemWalk& sw, int b, int T, int K, int greedy, const 
         path_ids[(size_t)b * T + t] = sw.ids[t][bj];
         pj = bj;
       }
-      score[b] = delta;
+      score[b] = (flags & kWalkFlagScoreLogits) ? delta + lse_sum(sw, T) : delta;
     }
   }
 }
@@ -387,8 +452,9 @@ template <bool kBf16>
 __global__ void __launch_bounds__(32 * kWarps)
     transition_walk_kernel(const int32_t* __restrict__ anchor, const int32_t* __restrict__ cand_ids,
                            const float* __restrict__ cand_lp, const void* __restrict__ Uv,
-                           const void* __restrict__ Vv, const float* __restrict__ gate, int T, int cand_rows,
-                           int first, int K, int R, int vocab, int greedy, SampleArgs sa,
+                           const void* __restrict__ Vv, const float* __restrict__ gate,
+                           const float* __restrict__ lse_rows, int T, int cand_rows, int first, int K, int R,
+                           int vocab, int walk_flags, SampleArgs sa,
                            int32_t* __restrict__ path_ids,
                            int32_t* __restrict__ path_idx, float* __restrict__ score, int32_t* err) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -405,13 +471,15 @@ __global__ void __launch_bounds__(32 * kWarps)
       sw.lp[t][j] = cand_lp[at];
     }
   }
+  for (int t = threadIdx.x; t < T; t += blockDim.x)
+    sw.lse[t] = lse_rows ? lse_rows[(size_t)b * cand_rows + first + t] : 0.f;
   __syncthreads();
   pad_candidates(sw, T, K);
   __syncthreads();
   build_tiles<kBf16>(sw, T, R, Uv, Vv, gate ? gate + ((size_t)b * cand_rows + first) * R : nullptr, stage);
   __syncthreads();
   if ((threadIdx.x >> 5) != 0) return;
-  walk_warp0(sw, b, T, K, greedy, sa, path_ids, path_idx, score);
+  walk_warp0(sw, b, T, K, walk_flags, sa, path_ids, path_idx, score);
 }
 
 // Bytes of one warp's merge staging: values and ids [parts][16], (max, sum) [parts], heads.
@@ -434,7 +502,7 @@ __global__ void __launch_bounds__(32 * kWarps)
                        const float2* __restrict__ part_ms, int parts, int M, const int32_t* __restrict__ anchor,
                        const void* __restrict__ Uv, const void* __restrict__ Vv, const float* __restrict__ gate,
                        int T, int rows_per_seq, int first, int K, int R, int vocab,
-                       int greedy, SampleArgs sa, int32_t* __restrict__ cand_ids, float* __restrict__ cand_lp,
+                       int walk_flags, SampleArgs sa, int32_t* __restrict__ cand_ids, float* __restrict__ cand_lp,
                        float* __restrict__ lse_out, int32_t* __restrict__ path_ids, int32_t* __restrict__ path_idx,
                        float* __restrict__ score, int32_t* err) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -499,7 +567,10 @@ __global__ void __launch_bounds__(32 * kWarps)
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
       const float lse = m + logf(s);
-      if (lane == 0 && lse_out) lse_out[slot] = lse;
+      if (lane == 0) {
+        sw.lse[t] = lse;
+        if (lse_out) lse_out[slot] = lse;
+      }
       warp_merge_lists(sv, si, head, parts, K, [&](int k, int32_t id, float v) {
         const float lp = v - lse;
         // every merged id indexes U and V below: a partial that held no column would carry an
@@ -533,12 +604,9 @@ __global__ void __launch_bounds__(32 * kWarps)
       const __nv_bfloat16* stA =
           warp == 0 ? a0 : reinterpret_cast<const __nv_bfloat16*>(region + (warp - 1) * wstride) + kKP * kRowPad;
       __nv_bfloat16* stB = reinterpret_cast<__nv_bfloat16*>(region + warp * wstride);
-      if (gate) {
-        gate_rows(stB, R, gate + ((size_t)b * rows_per_seq + first + warp) * R);
-        __syncwarp();
-      }
       float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      tile_mma(stA, stB, R, acc);
+      if (gate) tile_mma_gated(stA, stB, R, gate + ((size_t)b * rows_per_seq + first + warp) * R, acc);
+      else tile_mma(stA, stB, R, acc);
       store_tau(acc, sw.tau[warp]);
     }
     __syncthreads();
@@ -551,7 +619,7 @@ __global__ void __launch_bounds__(32 * kWarps)
     __syncthreads();
   }
   if (warp != 0) return;
-  walk_warp0(sw, b, T, K, greedy, sa, path_ids, path_idx, score);
+  walk_warp0(sw, b, T, K, walk_flags, sa, path_ids, path_idx, score);
 }
 
 constexpr size_t kWalkStageBytes = (size_t)kWarps * 2 * kKP * kRowPad * sizeof(__nv_bfloat16);
@@ -566,7 +634,7 @@ size_t select_walk_smem(int parts) {
 cudaError_t launch_select_walk(bool bf16, const float* part_val, const int32_t* part_id, const float* part_ms,
                                int parts, int M, const int32_t* anchor, const void* U, const void* V,
                                const float* gate, int B, int T, int rows_per_seq, int first, int K, int R,
-                               int vocab, int greedy, const float* uniforms, float inv_temp, int32_t* cand_ids,
+                               int vocab, int walk_flags, const float* uniforms, float inv_temp, int32_t* cand_ids,
                                float* cand_lp, float* lse, int32_t* path_ids, int32_t* path_idx, float* score,
                                int32_t* err, cudaStream_t s) {
   if (first < 0 || first + T > rows_per_seq) return cudaErrorInvalidValue;
@@ -592,7 +660,7 @@ cudaError_t launch_select_walk(bool bf16, const float* part_val, const int32_t* 
     e = smem_opt_in(reinterpret_cast<const void*>(select_walk_kernel<true>), smem_done);
     if (e != cudaSuccess) return e;
     e = cudaLaunchKernelEx(&cfg, select_walk_kernel<true>, part_val, part_id, ms, parts, M, anchor, U, V, gate, T,
-                           rows_per_seq, first, K, R, vocab, greedy, sa, cand_ids, cand_lp, lse, path_ids,
+                           rows_per_seq, first, K, R, vocab, walk_flags, sa, cand_ids, cand_lp, lse, path_ids,
                            path_idx, score, err);
     if (e != cudaSuccess) return e;
   } else {
@@ -600,7 +668,7 @@ cudaError_t launch_select_walk(bool bf16, const float* part_val, const int32_t* 
     e = smem_opt_in(reinterpret_cast<const void*>(select_walk_kernel<false>), smem_done);
     if (e != cudaSuccess) return e;
     e = cudaLaunchKernelEx(&cfg, select_walk_kernel<false>, part_val, part_id, ms, parts, M, anchor, U, V, gate, T,
-                           rows_per_seq, first, K, R, vocab, greedy, sa, cand_ids, cand_lp, lse, path_ids,
+                           rows_per_seq, first, K, R, vocab, walk_flags, sa, cand_ids, cand_lp, lse, path_ids,
                            path_idx, score, err);
     if (e != cudaSuccess) return e;
   }
@@ -608,8 +676,9 @@ cudaError_t launch_select_walk(bool bf16, const float* part_val, const int32_t* 
 }
 
 cudaError_t launch_transition_walk(bool bf16, const int32_t* anchor, const int32_t* cand_ids,
-                                   const float* cand_lp, const void* U, const void* V, const float* gate, int B,
-                                   int T, int cand_rows, int first, int K, int R, int vocab, int greedy,
+                                   const float* cand_lp, const void* U, const void* V, const float* gate,
+                                   const float* lse_rows, int B, int T, int cand_rows, int first, int K, int R,
+                                   int vocab, int walk_flags,
                                    const float* uniforms, float inv_temp, int32_t* path_ids, int32_t* path_idx,
                                    float* score, int32_t* err, cudaStream_t s) {
   if (first < 0 || first + T > cand_rows) return cudaErrorInvalidValue;
@@ -622,16 +691,16 @@ cudaError_t launch_transition_walk(bool bf16, const int32_t* anchor, const int32
     static unsigned char smem_done[64];
     e = smem_opt_in(reinterpret_cast<const void*>(transition_walk_kernel<true>), smem_done);
     if (e != cudaSuccess) return e;
-    transition_walk_kernel<true><<<B, 32 * kWarps, smem, s>>>(anchor, cand_ids, cand_lp, U, V, gate, T, cand_rows,
-                                                               first, K, R, vocab, greedy, sa, path_ids, path_idx,
-                                                               score, err);
+    transition_walk_kernel<true><<<B, 32 * kWarps, smem, s>>>(anchor, cand_ids, cand_lp, U, V, gate, lse_rows, T,
+                                                               cand_rows, first, K, R, vocab, walk_flags, sa,
+                                                               path_ids, path_idx, score, err);
   } else {
     static unsigned char smem_done[64];
     e = smem_opt_in(reinterpret_cast<const void*>(transition_walk_kernel<false>), smem_done);
     if (e != cudaSuccess) return e;
-    transition_walk_kernel<false><<<B, 32 * kWarps, smem, s>>>(anchor, cand_ids, cand_lp, U, V, gate, T,
-                                                                cand_rows, first, K, R, vocab, greedy, sa, path_ids,
-                                                                path_idx, score, err);
+    transition_walk_kernel<false><<<B, 32 * kWarps, smem, s>>>(anchor, cand_ids, cand_lp, U, V, gate, lse_rows, T,
+                                                                cand_rows, first, K, R, vocab, walk_flags, sa,
+                                                                path_ids, path_idx, score, err);
   }
   return cudaGetLastError();
 }

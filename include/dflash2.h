@@ -64,7 +64,8 @@ enum {
   DFLASH2_CONV_TAPS_RAW = 1u << 0,    /* taps used as projected, unnormalised */
   DFLASH2_WALK_VITERBI = 0,           /* default: exact best path (Viterbi) */
   DFLASH2_WALK_GREEDY = 1u << 1,      /* the pages' greedy walk: best successor at each step */
-  DFLASH2_FIRST_SLOT_1 = 1u << 2      /* row 0 of each block is the anchor's own position */
+  DFLASH2_FIRST_SLOT_1 = 1u << 2,     /* row 0 of each block is the anchor's own position */
+  DFLASH2_SCORE_LOGITS = 1u << 3      /* whole-tail calls: report the walk's score on raw logits */
 };
 
 /* Slots. By default all `block` rows of a sequence are slots and the anchor is the token
@@ -95,7 +96,8 @@ typedef struct {
   int32_t conv_kernel_size; /* conv taps (2) */
   int32_t conv_layers;      /* NL: conv layers chained (5) */
   int32_t dtype;            /* dflash2_dtype_t of hidden, lm_head, U, V, conv_w */
-  uint32_t flags;           /* DFLASH2_CONV_TAPS_* | DFLASH2_WALK_* */
+  uint32_t flags;           /* DFLASH2_CONV_TAPS_* | DFLASH2_WALK_* | DFLASH2_FIRST_SLOT_1 |
+                               DFLASH2_SCORE_LOGITS */
 } dflash2_shape_t;
 
 /* Bytes of workspace that every call below needs for `shape` on the current
@@ -136,8 +138,9 @@ dflash2_status_t dflash2_select_topk(const dflash2_shape_t* shape, const void* r
  * (the gate of the current slot t; for t = 0 the anchor is the previous token).
  * The gate is contracted in the LM-head pass itself (its R rows are appended to the head's
  * columns), so it costs no extra pass over the rows. gate_w has the call's dtype. In the walk,
- * V[cur_j, r] * gate[r] is rounded to bf16 once before the fp32-accumulated product with U
- * (fp32 embeddings keep it in fp32).
+ * V[cur_j, r] * gate[r] is formed in fp32 and split into two bf16 parts (hi = bf16 of the
+ * product, lo = bf16 of the remainder; together within about 2^-17 of the fp32 product), and
+ * both are contracted with U with fp32 accumulation (fp32 embeddings keep the product in fp32).
  *
  * dflash2_select_topk_gated: dflash2_select_topk plus gate [M, R] fp32 out (gate_w non-NULL;
  * gate_w NULL is dflash2_select_topk, gate ignored). */
@@ -190,7 +193,9 @@ dflash2_status_t dflash2_merge_partials(const dflash2_shape_t* shape, int32_t* c
  * delta_t(j) = lp_t(j) + max_i (delta_{t-1}(i) + tau_t(i, j)), fp32, every
  * argmax taking the lowest index; score = max_j delta_{T-1}(j).
  * Greedy (DFLASH2_WALK_GREEDY): j_t = argmax_j (lp_t(j) + tau_t(j_{t-1}, j)),
- * score accumulated along the path in the same order as the Viterbi recursion. */
+ * score accumulated along the path in the same order as the Viterbi recursion.
+ * DFLASH2_SCORE_LOGITS is accepted only by the whole-tail calls (the walk calls here, which take
+ * log-probabilities, return DFLASH2_ERR_UNSUPPORTED with it). */
 dflash2_status_t dflash2_viterbi(const dflash2_shape_t* shape, const int32_t* anchor,
                                  const int32_t* cand_ids, const float* cand_lp,
                                  const void* U, const void* V,
@@ -206,13 +211,19 @@ dflash2_status_t dflash2_viterbi_gated(const dflash2_shape_t* shape, const int32
                                        void* ws, size_t ws_bytes, void* stream);
 
 /* A path sampled at temperature T > 0 instead of the best one ("DFlash 2: keeping drafts
- * parallel", section "軽量パスセレクター": the walk can also sample from the same scores):
+ * parallel", section "軽量パスセレクター": the walk can also sample from the same scores).
+ * Two forms, by the shape's walk flag.
+ * Default (Viterbi flag): the whole path is drawn from the path distribution,
  * P(path) = exp(score(path) / T) / Z over the K^T paths, score(path) as for dflash2_viterbi
  * (with the context gate when gate is non-NULL, as in dflash2_viterbi_gated). Forward filtering
  * in fp32, alpha_0(j) = (lp_0(j) + tau_0(j)) / T, alpha_t(j) = lp_t(j) / T +
  * logsumexp_i (alpha_{t-1}(i) + tau_t(i, j) / T); then backward draws: j_{T-1} ~ softmax(alpha_{T-1}),
  * j_{t-1} ~ softmax_i (alpha_{t-1}(i) + tau_t(i, j_t) / T), each the smallest candidate index
  * whose cumulative probability exceeds uniforms[b, t] (slot t's draw, in [0, 1)).
+ * DFLASH2_WALK_GREEDY: the pages' walk with each step's arg-max replaced by a draw from the same
+ * step scores: j_0 ~ softmax_j ((lp_0(j) + tau_0(j)) / T), j_t ~ softmax_j ((lp_t(j) +
+ * tau_t(j_{t-1}, j)) / T), each the smallest index whose cumulative probability exceeds
+ * uniforms[b, t]; score receives sum_t log p_t(j_t), the log-probability of the drawn path.
  *   temperature > 0 (finite); uniforms [B, T] fp32 device: the caller's random numbers
  *   (the library draws none, so a result is reproducible from its inputs)
  *   score [B] fp32 receives log P(path) of the drawn path.
@@ -228,7 +239,12 @@ dflash2_status_t dflash2_sample_walk(const dflash2_shape_t* shape, const int32_t
  *   hidden [B, T, H], lm_head [V, H], U/V [V, R], conv_w [NL, 2H/16, H], anchor [B]
  *   path_ids, path_idx [B, T] int32; score [B] fp32
  *   cand_ids [B, T, K], cand_lp [B, T, K], lse [B, T]: optional copies of the
- *   intermediate candidates (NULL to skip). */
+ *   intermediate candidates (NULL to skip).
+ * With DFLASH2_SCORE_LOGITS the Viterbi / greedy score is reported on the head's raw logits
+ * (the pages' per-slot score is the drafter's own logit, "DFlash 2: keeping drafts parallel",
+ * section "軽量パスセレクター"): sum_t logit_t(j_t) + transitions = the log-softmax score plus
+ * sum_t lse_t, summed in fp32. The path is the same under either score (per-slot constants do
+ * not move an arg-max); a sampled walk's score stays log P(path). */
 dflash2_status_t dflash2_draft_tail(const dflash2_shape_t* shape, const void* hidden, const void* lm_head,
                                     const void* U, const void* V, const void* conv_w,
                                     const int32_t* anchor, int32_t* path_ids, int32_t* path_idx,

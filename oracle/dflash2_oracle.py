@@ -43,17 +43,19 @@ Readings where the pages are silent (each is a fixed choice, stated where used):
      head reads), gate_w [R, H]. The selector's +2.0M parameters of Table 2 fit one such
      [hidden x 256] map per embedding (3 x 2560 x 256 at the 4B target's hidden 2560).
   R9 the walk is a Viterbi (exact best path); the pages' greedy walk is kept as
-     ``greedy_walk`` for comparison; at temperature T > 0 a path is sampled from the same
-     scores (``sample_walk``: P(path) proportional to exp(score / T), forward filtering and
-     backward sampling, with the caller's uniform draws).
+     ``greedy_walk``; at temperature T > 0 a path is sampled from the same scores, either
+     as a whole (``sample_walk``: P(path) proportional to exp(score / T), forward filtering
+     and backward sampling) or step by step along the greedy walk (``greedy_sample_walk``:
+     each step drawn from the softmax of that step's scores), with the caller's uniform draws.
   R10 top-K order: logit descending, ties to the lower token id; Viterbi ties go
       to the lower candidate index.
   R12 storage: layer outputs are rounded to the input dtype (bf16 RNE or fp32);
       logits, log-softmax, transitions and path scores are fp32 values.
-Decisions that turn floats into integers (the top-K order, every Viterbi argmax) are
-taken in fp32, the precision the CUDA path takes them in: logits are formed in
-float64 and rounded once to fp32 before sorting; the Viterbi recursion adds and
-compares fp32 values in the order the recursion is written.
+Decisions that turn floats into integers (the top-K order, every Viterbi and greedy
+argmax) are taken in fp32, the precision the CUDA path takes them in: logits are formed
+in float64 and rounded once to fp32 before sorting; the Viterbi recursion adds and
+compares fp32 values in the order the recursion is written; each greedy step compares
+the fp32 sums lp_t(j) + tau_t(j_{t-1}, j). Scores of a chosen path are float64 sums.
 """
 from __future__ import annotations
 
@@ -307,30 +309,61 @@ def viterbi_two_best(cand_lp: np.ndarray, tau: np.ndarray):
 
 
 def greedy_walk(cand_lp: np.ndarray, tau: np.ndarray):
-    """The pages' walk (R9): from the anchor, take the best successor at each step, in fp32.
+    """The pages' walk (R9): from the anchor, take the best successor at each step.
 
     j_0 = argmax_j lp_0(j) + tau_0(0, j); j_t = argmax_j lp_t(j) + tau_t(j_{t-1}, j), lowest j on
-    ties. The score follows the Viterbi recursion's order along the chosen path:
-    d_0 = lp_0(j_0) + tau_0(0, j_0), d_t = lp_t(j_t) + (d_{t-1} + tau_t(j_{t-1}, j_t)).
-    Returns (path_idx [B,T] int32, score [B] float32)."""
+    ties. Each step's candidate scores are fp32 sums, the precision the arg-max is taken in (R12);
+    the returned score is the path's score in float64 (``path_score``).
+    Returns (path_idx [B,T] int32, score [B] float64)."""
     B, T, K = cand_lp.shape
     lp = cand_lp.astype(np.float32)
     tt = tau.astype(np.float32)
     path = np.zeros((B, T), dtype=np.int32)
-    score = np.zeros(B, dtype=np.float32)
     for b in range(B):
-        v = (lp[b, 0] + tt[b, 0, 0]).astype(np.float32)
-        j = int(np.argmax(v))
-        d = np.float32(v[j])
-        path[b, 0] = j
-        for t in range(1, T):
+        j = 0  # slot 0's predecessor is the anchor: every row of tau_0 is the same
+        for t in range(T):
             v = (lp[b, t] + tt[b, t, j]).astype(np.float32)
-            jn = int(np.argmax(v))
-            d = np.float32(lp[b, t, jn] + np.float32(d + tt[b, t, j, jn]))
-            j = jn
+            j = int(np.argmax(v))
             path[b, t] = j
-        score[b] = d
-    return path, score
+    return path, path_score(cand_lp, tau, path)
+
+
+def _inverse_cdf(p: np.ndarray, u: float):
+    """Smallest index whose cumulative probability exceeds u (candidates in index order), and the
+    distance from u to the nearest interior cumulative boundary (inf for a single candidate)."""
+    c = np.cumsum(p)
+    k = min(int(np.searchsorted(c, u, side="right")), len(p) - 1)
+    near = float(np.min(np.abs(c[:-1] - u))) if len(p) > 1 else np.inf
+    return k, near
+
+
+def greedy_sample_walk(cand_lp: np.ndarray, tau: np.ndarray, temperature: float, u: np.ndarray):
+    """The pages' sampling along the walk (R9, [P4] "各ステップで最良の後続を貪欲にたどり、同じスコア
+    からサンプリング"): the greedy walk with each step's arg-max replaced by a draw from the same
+    step scores at temperature T > 0, in float64:
+      j_0 ~ softmax_j ((lp_0(j) + tau_0(0, j)) / T),  j_t ~ softmax_j ((lp_t(j) + tau_t(j_{t-1}, j)) / T),
+    each by inverse CDF on u[b, t] (slot t's draw; the smallest index whose cumulative probability
+    exceeds it).
+    Returns (path_idx [B,T] int32, logprob [B] float64 = sum_t log p_t(j_t), cdf_margin [B] float64 =
+    the smallest distance between a draw and a cumulative-probability boundary along the path)."""
+    B, T, K = cand_lp.shape
+    lp = cand_lp.astype(np.float64)
+    tt = tau.astype(np.float64)
+    inv_t = 1.0 / float(temperature)
+    path = np.zeros((B, T), dtype=np.int32)
+    logp = np.zeros(B)
+    margin = np.full(B, np.inf)
+    for b in range(B):
+        j = 0
+        for t in range(T):
+            s = (lp[b, t] + tt[b, t, j]) * inv_t
+            p = np.exp(s - s.max())
+            p = p / p.sum()
+            j, near = _inverse_cdf(p, float(u[b, t]))
+            path[b, t] = j
+            logp[b] += np.log(p[j])
+            margin[b] = min(margin[b], near)
+    return path, logp, margin
 
 
 def sample_walk(cand_lp: np.ndarray, tau: np.ndarray, temperature: float, u: np.ndarray):
@@ -360,10 +393,7 @@ def sample_walk(cand_lp: np.ndarray, tau: np.ndarray, temperature: float, u: np.
 
     def draw(logw, uu):
         p = np.exp(logw - lse(logw))
-        c = np.cumsum(p)
-        k = int(np.searchsorted(c, uu, side="right"))
-        k = min(k, len(p) - 1)
-        near = np.min(np.abs(c[:-1] - uu)) if len(p) > 1 else np.inf
+        k, near = _inverse_cdf(p, uu)
         return k, float(np.log(p[k])), near
 
     for b in range(B):
@@ -423,7 +453,7 @@ def brute_force_best(cand_lp: np.ndarray, tau: np.ndarray):
 # ---------------------------------------------------------------------------
 
 
-def draft_tail(inp: dict, shape, seqs=None, row_block: int = 64) -> dict:
+def draft_tail(inp: dict, shape, seqs=None, row_block: int = 256) -> dict:
     """Run the whole tail for the listed sequences (all by default).
 
     inp: dict from synth.make_inputs; shape: synth.Shape. Returns per-sequence outputs:
@@ -438,7 +468,7 @@ def draft_tail(inp: dict, shape, seqs=None, row_block: int = 64) -> dict:
     return select_from_z(z, inp, shape, seqs, row_block)
 
 
-def select_from_z(z: np.ndarray, inp: dict, shape, seqs, row_block: int = 64) -> dict:
+def select_from_z(z: np.ndarray, inp: dict, shape, seqs, row_block: int = 256) -> dict:
     """The tail after the conv, on given conv outputs z [b, T, H] of the listed sequences:
     logits, lse, top-K, transitions from those sequences' anchors, Viterbi and margins.
     With shape.first_slot = 1 (R6) the slots are rows 1..T-1 and every per-slot output has

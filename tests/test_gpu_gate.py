@@ -63,6 +63,8 @@ def test_draft_tail_gated_greedy():
     gp, gs = O.greedy_walk(g["cand_lp"], tau)
     assert np.array_equal(g["path_idx"], gp)
     assert np.allclose(g["score"], gs, atol=P.SCORE_TOL)
+    P.check_walk(sh, inp["anchor"], inp["U"], inp["V"], g["cand_ids"], g["cand_lp"], g["path_idx"],
+                 g["path_ids"], g["score"], greedy=True, gate=g["gate"])
 
 
 @pytest.mark.parametrize("M,V,H,R", [(8, 31_040, 5120, 256), (200, 12_345, 256, 64), (1, 777, 64, 16)])

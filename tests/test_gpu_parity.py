@@ -77,6 +77,17 @@ def test_fp32_small_rows():
 # ------------------------------------------------------------------ per-step calls
 
 
+def _conv_parity(sh, inp):
+    """dflash2_conv on all layers and one layer per call, against the oracle (each layer on the
+    GPU's own layer input, and the chain end to end)."""
+    shape = P.shape_of(sh)
+    x, w = P.dev(inp["hidden"]), P.dev(inp["conv_w"])
+    z = P.run_conv(shape, x, w)
+    zl = P.run_conv_layers(shape, x, w)
+    ref = O.conv_chain(inp["hidden"], inp["conv_w"], sh.dtype, 16, sh.taps)
+    return P.check_conv_layers(inp["hidden"], inp["conv_w"], sh.dtype, sh.taps, zl, z, ref_chain=ref)
+
+
 # 8 and 16 rows run the chain kernel that reads whole rows per CTA; 40, 96 and 160 rows the
 # split-K chain (one row tile; one tile; two tiles with a 32-row tail)
 @pytest.mark.parametrize("layers,raw,batch", [(1, False, 1), (5, False, 1), (5, False, 2), (1, False, 5),
@@ -89,21 +100,14 @@ def test_conv_step(layers, raw, batch):
         sh.taps = "raw"
         rc.conv_std = 0.002  # keeps raw taps near unit scale
     inp = synth.make_inputs(rc, with_lm_head=True)
-    z_ref = O.conv_chain(inp["hidden"], inp["conv_w"], "bf16", 16, sh.taps)
-    z = P.run_conv(P.shape_of(sh), P.dev(inp["hidden"]), P.dev(inp["conv_w"]))
-    rep = P.check_conv(z, z_ref, x_in=inp["hidden"] if layers == 1 else None)
-    if layers == 1:
-        assert rep["conv_exact_frac"] > 0.95
-    print(rep)
+    print(_conv_parity(sh, inp))
 
 
 def test_conv_step_block16_many_rows():
     rc = _recipe(batch=40, block=16, hidden=1024, vocab=64, layers=5)
     sh = rc.shape
     inp = synth.make_inputs(rc)
-    z_ref = O.conv_chain(inp["hidden"], inp["conv_w"], "bf16", 16)
-    z = P.run_conv(P.shape_of(sh), P.dev(inp["hidden"]), P.dev(inp["conv_w"]))
-    P.check_conv(z, z_ref)
+    print(_conv_parity(sh, inp))
 
 
 # at most 8 rows in the chain kernel: sequences shorter than the rows (a sequence start inside
@@ -118,9 +122,7 @@ def test_conv_step_few_rows(batch, block, hidden, layers, raw):
         sh.taps = "raw"
         rc.conv_std = 0.002
     inp = synth.make_inputs(rc)
-    z_ref = O.conv_chain(inp["hidden"], inp["conv_w"], "bf16", 16, sh.taps)
-    z = P.run_conv(P.shape_of(sh), P.dev(inp["hidden"]), P.dev(inp["conv_w"]))
-    print(P.check_conv(z, z_ref, x_in=inp["hidden"] if layers == 1 else None))
+    print(_conv_parity(sh, inp))
 
 
 @pytest.mark.parametrize("batch,block,hidden,layers", [(11, 12, 512, 3), (1, 8, 1088, 2), (4, 5, 1088, 2)])
@@ -131,9 +133,7 @@ def test_conv_step_tile_edges(batch, block, hidden, layers):
     rc = _recipe(batch=batch, block=block, hidden=hidden, vocab=64, layers=layers)
     sh = rc.shape
     inp = synth.make_inputs(rc)
-    z_ref = O.conv_chain(inp["hidden"], inp["conv_w"], "bf16", 16)
-    z = P.run_conv(P.shape_of(sh), P.dev(inp["hidden"]), P.dev(inp["conv_w"]))
-    print(P.check_conv(z, z_ref))
+    print(_conv_parity(sh, inp))
 
 
 @pytest.mark.parametrize("B", [1, 2])
@@ -274,3 +274,38 @@ def test_argument_errors_return_before_launch():
     assert st == df2.ERR_INVALID_ARGUMENT
     torch.cuda.synchronize()
     assert df2.read_device_error(ws) == 0
+
+
+@pytest.mark.parametrize("greedy", [False, True])
+def test_draft_tail_score_on_logits(greedy):
+    # DFLASH2_SCORE_LOGITS: same candidates and path; the score is the log-softmax score plus the
+    # slots' lse (the pages' per-slot score is the drafter's raw logit)
+    import block_drafter_dflash2_gb300 as df2
+    rc = _recipe(batch=3, block=8, hidden=512, vocab=20_011, layers=2)
+    sh = rc.shape
+    inp = synth.make_inputs(rc)
+    d = P.upload_inputs(inp)
+    base = P.shape_of(sh, greedy=greedy)
+    flagged = df2.Shape.make(sh.batch, sh.block, sh.hidden, sh.vocab, sh.top_k, sh.rank, sh.layers,
+                             greedy=greedy, score_logits=True)
+    g0 = P.run_tail(base, d)
+    g1 = P.run_tail(flagged, d)
+    for k in ("path_ids", "path_idx", "cand_ids", "cand_lp", "lse"):
+        assert np.array_equal(g0[k], g1[k]), k
+    lse_sum = g1["lse"].astype(np.float64).sum(axis=1)
+    assert np.allclose(g1["score"].astype(np.float64), g0["score"].astype(np.float64) + lse_sum, atol=1e-4, rtol=0)
+    # against the oracle end to end: its path score on its own raw logits
+    ref = O.draft_tail(inp, sh)
+    raw = O.path_score(ref["cand_logit"].astype(np.float64), ref["tau"], ref["path_idx"]) if not greedy else None
+    if raw is not None:
+        for b in range(sh.batch):
+            if np.array_equal(g1["path_idx"][b], ref["path_idx"][b]):
+                assert abs(float(g1["score"][b]) - raw[b]) <= P.SCORE_TOL
+    # the walk-only call has no lse: the flag is refused there
+    ws = P.workspace(flagged)
+    B, T, K = sh.batch, sh.block, sh.top_k
+    o = [torch.empty((B, T), dtype=torch.int32, device="cuda"), torch.empty((B, T), dtype=torch.int32, device="cuda"),
+         torch.empty((B,), dtype=torch.float32, device="cuda")]
+    with pytest.raises(df2.DFlash2Error) as e:
+        df2.viterbi(flagged, d["anchor"], P.dev(g1["cand_ids"]), P.dev(g1["cand_lp"]), d["U"], d["V"], *o, ws)
+    assert e.value.status == df2.ERR_UNSUPPORTED

@@ -15,11 +15,7 @@ from tests import parity as P
 
 pytestmark = pytest.mark.gpu
 
-LOGP_TOL = 2e-3   # log P(path): fp32 forward filtering against float64
-# With the context gate the walk rounds V (.) g to bf16 once (2^-9 relative per term): at
-# |U|, |V| ~ 0.2, |g| ~ 1 and rank 256 that is ~1e-3 per tau entry, summed over 8 slots and
-# log Z, so the gated band is 1e-2.
-LOGP_TOL_GATED = 1e-2
+LOGP_TOL = 2e-3   # log P(path): fp32 forward filtering against float64 (gated or not)
 CDF_BAND = 1e-4   # a draw this close to a cumulative-probability boundary may fall either side
 
 
@@ -28,6 +24,37 @@ def _lib():
     import block_drafter_dflash2_gb300 as df2
     assert torch.cuda.is_available()
     df2.load()
+
+
+def greedy_step_logp(lp, tau, temp, path):
+    """log P of given paths under per-step sampling along the greedy walk, written out in float64:
+    sum_t log softmax_j ((lp_t(j) + tau_t(j_{t-1}, j)) / T)(j_t), slot 0's predecessor the anchor."""
+    B, T, K = lp.shape
+    out = np.zeros(B)
+    for b in range(B):
+        prev = 0
+        for t in range(T):
+            s = (lp[b, t].astype(np.float64) + tau[b, t, prev].astype(np.float64)) / temp
+            out[b] += s[path[b, t]] - np.logaddexp.reduce(s)
+            prev = int(path[b, t])
+    return out
+
+
+def check_greedy_sample(cand, lp, tau, temp, u, g_pix, g_pid, g_logp, logp_tol=LOGP_TOL):
+    """Per-step draws along the greedy walk: exact except where the oracle's draw lies within
+    CDF_BAND of a boundary; the GPU's log P matches the exact value for the path it drew."""
+    B, T, K = lp.shape
+    o_pix, _, margin = O.greedy_sample_walk(lp, tau, temp, u)
+    exact = greedy_step_logp(lp, tau, temp, g_pix)
+    near = 0
+    for b in range(B):
+        assert np.array_equal(g_pid[b], cand[b, np.arange(T), g_pix[b]])
+        if margin[b] > CDF_BAND:
+            assert np.array_equal(g_pix[b], o_pix[b]), f"seq {b}: drew {g_pix[b]} vs {o_pix[b]}"
+        elif not np.array_equal(g_pix[b], o_pix[b]):
+            near += 1
+        assert abs(float(g_logp[b]) - exact[b]) <= logp_tol, f"seq {b}: log P {g_logp[b]} vs {exact[b]}"
+    return near
 
 
 def _run_sample(shape, anchor, cand, lp, U, V, temp, u, gate=None):
@@ -93,7 +120,7 @@ def test_sample_walk_gated():
     u = rng.random((B, T)).astype(np.float32)
     pid, pix, sc = _run_sample(P.shape_of(sh), anchor, cand, lp, U, V, 1.0, u, gate=gate)
     tau = O.transitions(anchor, cand, U, V, gate)
-    check_sample(cand, lp, tau, 1.0, u.astype(np.float64), pix, pid, sc, logp_tol=LOGP_TOL_GATED)
+    check_sample(cand, lp, tau, 1.0, u.astype(np.float64), pix, pid, sc, logp_tol=LOGP_TOL)
 
 
 def test_sampler_distribution_over_many_draws():
@@ -138,15 +165,15 @@ def test_low_temperature_sample_is_the_viterbi_path():
             assert np.array_equal(pix[b], vix[b])
 
 
-@pytest.mark.parametrize("gated", [False, True])
-def test_draft_tail_sampled_small(gated):
+@pytest.mark.parametrize("gated,greedy", [(False, False), (True, False), (False, True), (True, True)])
+def test_draft_tail_sampled_small(gated, greedy):
     import block_drafter_dflash2_gb300 as df2
     rc = synth.scaled_recipe(synth.recipe(2), batch=6, block=8, hidden=512, vocab=30_011, layers=2)
     sh = rc.shape
     inp = synth.make_inputs(rc)
     B, T, K, R = sh.batch, sh.block, sh.top_k, sh.rank
     d = P.upload_inputs(inp)
-    shape = P.shape_of(sh)
+    shape = P.shape_of(sh, greedy=greedy)
     u = np.random.default_rng(55).random((B, T)).astype(np.float32)
     o = {k: torch.empty(v, dtype=dt, device="cuda:0") for k, v, dt in
          [("pid", (B, T), torch.int32), ("pix", (B, T), torch.int32), ("sc", (B,), torch.float32),
@@ -160,5 +187,89 @@ def test_draft_tail_sampled_small(gated):
     cand, lp = P.host(o["ids"]), P.host(o["lp"])
     gate = P.host(o["gate"]) if gated else None
     tau = O.transitions(inp["anchor"], cand, inp["U"], inp["V"], gate)
-    check_sample(cand, lp, tau, 0.9, u.astype(np.float64), P.host(o["pix"]), P.host(o["pid"]), P.host(o["sc"]),
-                 logp_tol=LOGP_TOL_GATED if gated else LOGP_TOL)
+    check = check_greedy_sample if greedy else check_sample
+    check(cand, lp, tau, 0.9, u.astype(np.float64), P.host(o["pix"]), P.host(o["pid"]), P.host(o["sc"]))
+
+
+# ---------------------------------------------------------------- per-step draws along the greedy walk
+
+
+@pytest.mark.parametrize("T,K,R,temp", [(8, 16, 256, 1.0), (8, 16, 256, 0.3), (1, 16, 64, 2.0),
+                                        (16, 4, 64, 1.0), (3, 16, 384, 0.7)])
+def test_greedy_sample_walk_step(T, K, R, temp):
+    rng = np.random.default_rng(T * 100 + K + R + 1)
+    B, Vv = 64, 3000
+    sh = synth.Shape(batch=B, block=T, hidden=64, vocab=Vv, top_k=K, rank=R, layers=0)
+    U = synth.normal(19, 3, (Vv, R), 0.3)
+    V = synth.normal(19, 4, (Vv, R), 0.3)
+    cand = rng.integers(0, Vv, size=(B, T, K)).astype(np.int32)
+    lp = (-np.sort(np.abs(rng.standard_normal((B, T, K))), axis=2) * 1.5).astype(np.float32)
+    anchor = rng.integers(0, Vv, size=B).astype(np.int32)
+    u = rng.random((B, T)).astype(np.float32)
+    pid, pix, sc = _run_sample(P.shape_of(sh, greedy=True), anchor, cand, lp, U, V, temp, u)
+    tau = O.transitions(anchor, cand, U, V)
+    near = check_greedy_sample(cand, lp, tau, temp, u.astype(np.float64), pix, pid, sc)
+    print(T, K, R, temp, "draws at a boundary", near)
+
+
+def test_greedy_sample_walk_gated():
+    rng = np.random.default_rng(22)
+    B, T, K, R, Vv = 32, 8, 16, 256, 2000
+    sh = synth.Shape(batch=B, block=T, hidden=64, vocab=Vv, top_k=K, rank=R, layers=0)
+    U = synth.normal(10, 3, (Vv, R), 0.2)
+    V = synth.normal(10, 4, (Vv, R), 0.2)
+    cand = rng.integers(0, Vv, size=(B, T, K)).astype(np.int32)
+    lp = (-np.sort(np.abs(rng.standard_normal((B, T, K))), axis=2)).astype(np.float32)
+    anchor = rng.integers(0, Vv, size=B).astype(np.int32)
+    gate = rng.standard_normal((B, T, R)).astype(np.float32)
+    u = rng.random((B, T)).astype(np.float32)
+    pid, pix, sc = _run_sample(P.shape_of(sh, greedy=True), anchor, cand, lp, U, V, 1.0, u, gate=gate)
+    tau = O.transitions(anchor, cand, U, V, gate)
+    check_greedy_sample(cand, lp, tau, 1.0, u.astype(np.float64), pix, pid, sc)
+
+
+def test_greedy_sampler_distribution_over_many_draws():
+    # one 3-candidate, 2-slot lattice repeated over 6000 sequences with independent uniforms: the
+    # drawn paths' frequencies match the product of the step softmaxes
+    rng = np.random.default_rng(34)
+    B, T, K, R, Vv = 6000, 2, 3, 16, 50
+    sh = synth.Shape(batch=B, block=T, hidden=64, vocab=Vv, top_k=K, rank=R, layers=0)
+    U = synth.normal(13, 3, (Vv, R), 0.5)
+    V = synth.normal(13, 4, (Vv, R), 0.5)
+    cand = np.broadcast_to(rng.integers(0, Vv, size=(1, T, K)), (B, T, K)).astype(np.int32).copy()
+    lp = np.broadcast_to(-np.sort(np.abs(rng.standard_normal((1, T, K))), axis=2), (B, T, K)).astype(np.float32).copy()
+    anchor = np.full(B, 9, np.int32)
+    u = rng.random((B, T)).astype(np.float32)
+    temp = 0.8
+    pid, pix, sc = _run_sample(P.shape_of(sh, greedy=True), anchor, cand, lp, U, V, temp, u)
+    tau = O.transitions(anchor[:1], cand[:1], U, V)
+    paths = list(itertools.product(range(K), repeat=T))
+    prob = np.exp(np.array([greedy_step_logp(lp[:1], tau, temp, np.asarray(c)[None])[0] for c in paths]))
+    freq = np.array([np.mean(np.all(pix == np.asarray(c)[None], axis=1)) for c in paths])
+    assert abs(prob.sum() - 1.0) < 1e-9
+    assert np.all(np.abs(freq - prob) <= 4.5 * np.sqrt(prob * (1 - prob) / B) + 1e-3), (freq, prob)
+
+
+def test_low_temperature_greedy_sample_is_the_greedy_path():
+    rng = np.random.default_rng(45)
+    B, T, K, R, Vv = 16, 8, 16, 64, 2000
+    sh = synth.Shape(batch=B, block=T, hidden=64, vocab=Vv, top_k=K, rank=R, layers=0)
+    U = synth.normal(14, 3, (Vv, R), 0.3)
+    V = synth.normal(14, 4, (Vv, R), 0.3)
+    cand = rng.integers(0, Vv, size=(B, T, K)).astype(np.int32)
+    lp = (-np.sort(np.abs(rng.standard_normal((B, T, K))), axis=2) * 3).astype(np.float32)
+    anchor = rng.integers(0, Vv, size=B).astype(np.int32)
+    u = (rng.random((B, T)) * 0.9 + 0.05).astype(np.float32)
+    pid, pix, sc = _run_sample(P.shape_of(sh, greedy=True), anchor, cand, lp, U, V, 1e-3, u)
+    tau = O.transitions(anchor, cand, U, V)
+    gp, _ = O.greedy_walk(lp, tau)
+    for b in range(B):
+        # a clear best step everywhere along the greedy path: all the mass at T = 1e-3
+        gaps = []
+        prev = 0
+        for t in range(T):
+            v = np.sort(lp[b, t].astype(np.float64) + tau[b, t, prev])[::-1]
+            gaps.append(v[0] - v[1])
+            prev = gp[b, t]
+        if min(gaps) > 0.05:
+            assert np.array_equal(pix[b], gp[b])

@@ -4,6 +4,7 @@ and hand-worked values — never against the oracle itself.
 Each test names the definition it pins (DFlash2 pages: the conv "inside each block",
 the selector's pairwise score and walk from the anchor; see the oracle's header).
 """
+import itertools
 import json
 import math
 import os
@@ -357,7 +358,26 @@ def test_viterbi_equals_brute_force(K, T):
                        for c in itertools.product(range(K), repeat=T)), reverse=True)
         assert abs(allv[1] - second[b]) < 1e-9
     gp, gs = O.greedy_walk(lp, tau)
-    assert np.all(gs <= bs + 1e-5)  # greedy score is fp32; the brute-force maximum is float64
+    assert np.all(gs <= bs + 1e-12)  # no path scores above the brute-force maximum
+    # the greedy path by enumeration: among all paths, the one whose every step is the best
+    # successor of the step before (lowest index on ties), and its float64 score
+    for b in range(B):
+        steps = []
+        for combo in itertools.product(range(K), repeat=T):
+            ok = True
+            for t in range(T):
+                prev = 0 if t == 0 else combo[t - 1]
+                row = [float(np.float32(lp[b, t, j] + tau[b, t, prev, j])) for j in range(K)]
+                if combo[t] != row.index(max(row)):
+                    ok = False
+                    break
+            if ok:
+                steps.append(combo)
+        assert len(steps) == 1 and tuple(gp[b]) == steps[0]
+        s = float(lp[b, 0, gp[b, 0]]) + float(tau[b, 0, 0, gp[b, 0]])
+        for t in range(1, T):
+            s += float(lp[b, t, gp[b, t]]) + float(tau[b, t, gp[b, t - 1], gp[b, t]])
+        assert abs(gs[b] - s) < 1e-12
 
 
 def test_viterbi_zero_transitions_is_per_slot_argmax():
@@ -525,3 +545,84 @@ def test_tiny_fp32_workload_end_to_end_brute_force():
         lse = math.log(sum(math.exp(float(x)) for x in direct))
         assert abs(out["lse"].reshape(-1)[m] - lse) < 1e-9
     assert out["best"][0] >= out["second"][0]
+
+
+# ---------------------------------------------------------------- draw margins and per-step sampling
+
+
+def test_sample_walk_cdf_margin_hand_lattice():
+    # one slot, probabilities (0.5, 0.3, 0.2): cumulative boundaries at 0.5 and 0.8; the margin is
+    # the distance from u to the nearer of the two, and the draw is the first index past u
+    lp = np.log(np.array([[[0.5, 0.3, 0.2]]]))
+    tau = np.zeros((1, 1, 3, 3))
+    for u, idx, margin in ((0.55, 1, 0.05), (0.79, 1, 0.01), (0.85, 2, 0.05), (0.1, 0, 0.4), (0.5, 1, 0.0)):
+        p, _, m = O.sample_walk(lp, tau, 1.0, np.array([[u]]))
+        assert p[0, 0] == idx and abs(m[0] - margin) < 1e-12, (u, p, m)
+    # two slots without transitions: each slot's draw uses its own u and the margin is the smaller
+    # of the two slots' margins (slot 1 has boundaries at 0.25 and 0.75)
+    lp2 = np.log(np.array([[[0.5, 0.3, 0.2], [0.25, 0.5, 0.25]]]))
+    tau2 = np.zeros((1, 2, 3, 3))
+    p, _, m = O.sample_walk(lp2, tau2, 1.0, np.array([[0.55, 0.7]]))
+    assert p[0].tolist() == [1, 1] and abs(m[0] - 0.05) < 1e-12
+    p, _, m = O.sample_walk(lp2, tau2, 1.0, np.array([[0.3, 0.74]]))
+    assert p[0].tolist() == [0, 1] and abs(m[0] - 0.01) < 1e-12
+    # with a transition, slot 0 is drawn from its distribution given slot 1's draw: K = 2,
+    # lp_0 = log(1/2, 1/2), lp_1 = 0, tau_1(i, j) = log 3 for (i, j) = (1, 0), else 0. Slot 1's
+    # marginal is (2/3, 1/3); given j_1 = 0, slot 0 is (1/4, 3/4), boundary 0.25
+    lp3 = np.array([[[math.log(0.5), math.log(0.5)], [0.0, 0.0]]])
+    tau3 = np.zeros((1, 2, 2, 2))
+    tau3[0, 1, 1, 0] = math.log(3.0)
+    p, logp, m = O.sample_walk(lp3, tau3, 1.0, np.array([[0.3, 0.6]]))
+    assert p[0].tolist() == [1, 0]
+    assert abs(m[0] - min(abs(0.6 - 2 / 3), abs(0.3 - 0.25))) < 1e-12
+    assert abs(logp[0] - math.log(2 / 3 * 3 / 4)) < 1e-12
+
+
+def test_greedy_sample_walk_cdf_margin_and_draws_hand_lattice():
+    # per-step draws: slot 0 from softmax(lp_0 + tau_0), slot t from softmax(lp_t + tau_t(j_{t-1}, .))
+    lp = np.array([[[math.log(0.5), math.log(0.5)], [0.0, 0.0]]])
+    tau = np.zeros((1, 2, 2, 2))
+    tau[0, 1, 1, 0] = math.log(3.0)  # after candidate 1, slot 1 is (3/4, 1/4); after 0, (1/2, 1/2)
+    p, logp, m = O.greedy_sample_walk(lp, tau, 1.0, np.array([[0.6, 0.7]]))
+    assert p[0].tolist() == [1, 0] and abs(logp[0] - math.log(0.5 * 0.75)) < 1e-12
+    assert abs(m[0] - min(abs(0.6 - 0.5), abs(0.7 - 0.75))) < 1e-12
+    p, logp, m = O.greedy_sample_walk(lp, tau, 1.0, np.array([[0.4, 0.7]]))
+    assert p[0].tolist() == [0, 1] and abs(logp[0] - math.log(0.25)) < 1e-12
+    assert abs(m[0] - 0.1) < 1e-12
+    # temperature 2 halves every score: slot 1 after candidate 1 is (sqrt3, 1) / (sqrt3 + 1)
+    p, logp, _ = O.greedy_sample_walk(lp, tau, 2.0, np.array([[0.9, 0.62]]))
+    q = math.sqrt(3.0) / (math.sqrt(3.0) + 1.0)
+    assert p[0].tolist() == [1, 0] and abs(logp[0] - math.log(0.5 * q)) < 1e-12
+
+
+def test_greedy_sample_walk_distribution_is_product_of_step_softmaxes():
+    # draws on a regular grid of u reproduce P(path) = prod_t softmax_j(s_t(j_{t-1}, j) / T)(j_t),
+    # the step probabilities written out here by enumeration
+    lp, tau = _lattice(11, B=1, T=2, K=3)
+    temp = 0.9
+    paths = list(itertools.product(range(3), repeat=2))
+
+    def step_p(t, prev, j):
+        w = [math.exp((float(lp[0, t, c]) + float(tau[0, t, prev, c])) / temp) for c in range(3)]
+        return w[j] / sum(w)
+    prob = np.array([step_p(0, 0, c[0]) * step_p(1, c[0], c[1]) for c in paths])
+    n = 200
+    counts = {c: 0 for c in paths}
+    for a in range(n):
+        for c in range(n):
+            u = np.array([[(a + 0.5) / n, (c + 0.5) / n]])
+            pth, logp, _ = O.greedy_sample_walk(lp, tau, temp, u)
+            key = tuple(int(x) for x in pth[0])
+            counts[key] += 1
+            assert abs(logp[0] - math.log(prob[paths.index(key)])) < 1e-9
+    freq = np.array([counts[c] for c in paths]) / n ** 2
+    assert np.abs(freq - prob).max() < 0.02
+
+
+def test_greedy_sample_walk_low_temperature_is_greedy():
+    lp, tau = _lattice(12, B=3, T=5, K=4)
+    rng = np.random.default_rng(13)
+    gp, _ = O.greedy_walk(lp, tau)
+    for _ in range(5):
+        p, _, _ = O.greedy_sample_walk(lp, tau, 1e-4, rng.random((3, 5)) * 0.98 + 0.01)
+        assert np.array_equal(p, gp)

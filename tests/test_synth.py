@@ -1,6 +1,7 @@
 """The seeded input generator: Philox4x32-10 known-answer vectors (Salmon et al., SC'11,
 published test vectors), distribution moments, determinism and the bf16 rounding."""
 import numpy as np
+import pytest
 
 import synth
 from oracle import core as O
@@ -40,3 +41,48 @@ def test_hidden_rows_rms_normalised():
     h = O.widen(inp["hidden"])
     rms = np.sqrt((h * h).mean(axis=-1))
     assert np.allclose(rms, 1.0, atol=1e-2)
+
+
+def test_conv_comparator_catches_planted_errors():
+    # the comparator used by the GPU tests, fed the oracle's own per-layer outputs with a mistake
+    # planted in them: one element of a middle layer 3 % of its scale off, one element of a layer
+    # three bf16 units of its operands off (the bound is two), one whole channel of the chain
+    # output scaled by 1.5, and a chain output that differs from its last layer by one unit
+    from oracle import core as O
+    from tests import parity as P
+    rc = synth.scaled_recipe(synth.recipe(2), batch=2, block=8, hidden=256, vocab=64, layers=3)
+    inp = synth.make_inputs(rc)
+    h, w = inp["hidden"], inp["conv_w"]
+    layers = []
+    x = h
+    for l in range(3):
+        x = O.conv_chain(x, w[l:l + 1], "bf16", 16)
+        layers.append(x)
+    ref = O.conv_chain(h, w, "bf16", 16)
+    P.check_conv_layers(h, w, "bf16", "softmax", layers, layers[-1], ref_chain=ref)  # the oracle itself: passes
+
+    def planted(l, fn):
+        out = [a.copy() for a in layers]
+        v = O.widen(out[l]).copy()
+        fn(v, O.widen(h if l == 0 else layers[l - 1]))
+        out[l] = O.round_bf16(v)
+        return out
+    bad = planted(1, lambda v, x: v.__setitem__((1, 5, 17), v[1, 5, 17] + 0.03 * max(
+        np.sqrt(np.mean(v[1, 5] ** 2)), abs(v[1, 5, 17]), abs(x[1, 5, 17]), abs(x[1, 4, 17]))))
+    with pytest.raises(AssertionError):
+        P.check_conv_layers(h, w, "bf16", "softmax", bad, bad[-1], ref_chain=ref)
+
+    def three_units(v, x):
+        op = max(abs(x[0, 3, 40]), abs(x[0, 2, 40]))
+        v[0, 3, 40] += 3 * float(P.bf16_ulp(np.array([op]))[0])
+    bad = planted(0, three_units)
+    with pytest.raises(AssertionError):
+        P.check_conv_layers(h, w, "bf16", "softmax", bad, bad[-1], ref_chain=ref)
+    chain = O.widen(layers[-1]).copy()
+    chain[:, :, 99] *= 1.5
+    with pytest.raises(AssertionError):
+        P.check_conv_layers(h, w, "bf16", "softmax", layers, O.round_bf16(chain), ref_chain=ref)
+    chain = layers[-1].copy()
+    chain[0, 0, 0] ^= 1
+    with pytest.raises(AssertionError):
+        P.check_conv_layers(h, w, "bf16", "softmax", layers, chain, ref_chain=ref)

@@ -23,12 +23,13 @@ def _inputs(M, V, H, seed):
     return rc.shape, inp["hidden"].reshape(M, H), inp["lm_head"]
 
 
-def _call_noalloc(lib, shape, rows, lm_head, M, K):
+def _call_noalloc(lib, shape, rows, lm_head, M, K, with_lse=True):
     ids = torch.full((M, K), -1, dtype=torch.int32, device="cuda:0")
     lp = torch.full((M, K), float("nan"), dtype=torch.float32, device="cuda:0")
     lse = torch.full((M,), float("nan"), dtype=torch.float32, device="cuda:0")
     st = lib.dflash2_select_topk_noalloc(ctypes.byref(shape), rows.data_ptr(), lm_head.data_ptr(), ids.data_ptr(),
-                                         lp.data_ptr(), lse.data_ptr(), torch.cuda.current_stream().cuda_stream)
+                                         lp.data_ptr(), lse.data_ptr() if with_lse else None,
+                                         torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
     assert st == 0, f"status {st}"
     return P.host(ids), P.host(lp), P.host(lse)
@@ -48,6 +49,10 @@ def test_noalloc_matches_workspace_call_twice():
             assert np.array_equal(ids, ids_ref)
             assert np.abs(lp - lp_ref).max() <= P.LP_TOL
             assert np.abs(lse - lse_ref).max() <= P.LSE_TOL
+        # without an lse output (the merge keeps it in the scratch): same ids and log-probs
+        ids_n, lp_n, _ = _call_noalloc(lib, shape, d_rows, d_w, M, sh.top_k, with_lse=False)
+        assert np.array_equal(ids_n, ids_ref)
+        assert np.abs(lp_n - lp_ref).max() <= P.LP_TOL
         # and it is the right selection: same comparator as the other top-K tests
         l32 = O.logits(rows, lm_head)
         i_o, v_o, _ = O.topk_rows(l32, sh.top_k)
