@@ -60,16 +60,19 @@ def parse():
                     help="time one kernel alone (profiling case) instead of the whole tail")
     ap.add_argument("--rows", type=int, default=8, help="--kernel: rows of the contraction")
     ap.add_argument("--vocab", type=int, default=62080, help="--kernel: vocabulary size")
+    ap.add_argument("--oracle-child", type=int, default=None, help=argparse.SUPPRESS)
     return ap.parse_args()
 
 
 def peaks():
+    """(HBM GB/s, bf16 TFLOP/s burst, bf16 TFLOP/s sustained, source)."""
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             p = json.load(f)
-        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+        return (float(p["hbm_gbs"]), float(p["bf16_tflops"]),
+                float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured")
     except Exception:
-        return 6800.0, 1900.0, "fallback"
+        return 6800.0, 1900.0, 1700.0, "fallback"
 
 
 # ---------------------------------------------------------------------------------- clocks
@@ -151,17 +154,6 @@ def synth_uniforms(B: int, T: int):
     return synth.uniform(7, 40, B * T).reshape(B, T)
 
 
-def hidden_for_batch(rc, batch: int, lm_head):
-    """Hidden rows for another batch size with the same recipe (weights shared)."""
-    import synth
-    r2 = synth.scaled_recipe(rc, batch=batch)
-    r2.seed = rc.seed + 100 + batch
-    h = synth.normal(r2.seed, synth.TID_HIDDEN, (batch, rc.shape.block, rc.shape.hidden), 1.0, "f64")
-    h = h / np.sqrt(np.mean(h * h, axis=-1, keepdims=True) + 1e-6)
-    anchor = synth.uniform_int(r2.seed, synth.TID_ANCHOR, batch, rc.shape.vocab).astype(np.int32)
-    return synth.f64_to_bf16(h), anchor
-
-
 def lmhead_alg_bytes(sh, M):
     """Algorithmic bytes of one LM-head contraction launch: the weight stream, the rows,
     and the partials written (per-partition top-16 + (max, sum) per row)."""
@@ -219,7 +211,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     df2.load()
-    bw, tf, peak_kind = peaks()
+    bw, tf, tf_sus, peak_kind = peaks()
     rc, inp = make_workload(args.config)
     sh = rc.shape
     B, T, H, K = sh.batch, sh.block, sh.hidden, sh.top_k
@@ -338,21 +330,27 @@ def run_ours(args, rank, world, local_rank):
     assert np.array_equal(h_out[:B * T].numpy().reshape(B, T), out["pid"].cpu().numpy())
     e2e_total = max_over_ranks(sum(e2e_ms), dev)
 
-    # other batch sizes of the metric (weights shared with the main workload)
+    # the other workloads of the metric, each on its own seeded inputs (weights included):
+    # B=8 with planted peaks, B=32 with duplicated anchors, and the B=64 block-16 stress case
+    # (1024 rows into the LM head: past the ridge, tensor-bound)
     extra = {}
     if not args.no_extra and world == 1:
-        for b2 in (8, 32):
-            hb, ab = hidden_for_batch(rc, b2, inp["lm_head"])
-            hb_d, ab_d = up(hb), up(ab)
-            shp2 = df2.Shape.make(b2, T, H, sh.vocab, K, sh.rank, sh.layers)
+        for cfg in (3, 4, 5):
+            rc_c, inp_c = make_workload(cfg)
+            sh_c = rc_c.shape
+            Bc, Tc = sh_c.batch, sh_c.block
+            Mc = Bc * Tc
+            dc = {k: up(inp_c[k]) for k in ("hidden", "lm_head", "U", "V", "conv_w", "anchor")}
+            del inp_c
+            shp2 = df2.Shape.make(Bc, Tc, H, sh_c.vocab, K, sh_c.rank, sh_c.layers)
             ws2 = torch.zeros(df2.workspace_size(shp2), dtype=torch.uint8, device=dev)
-            o2 = dict(pid=torch.empty((b2, T), dtype=torch.int32, device=dev),
-                      pix=torch.empty((b2, T), dtype=torch.int32, device=dev),
-                      score=torch.empty((b2,), dtype=torch.float32, device=dev))
+            o2 = dict(pid=torch.empty((Bc, Tc), dtype=torch.int32, device=dev),
+                      pix=torch.empty((Bc, Tc), dtype=torch.int32, device=dev),
+                      score=torch.empty((Bc,), dtype=torch.float32, device=dev))
 
-            def call2(shp2=shp2, o2=o2, ws2=ws2, hb_d=hb_d, ab_d=ab_d):
-                df2.draft_tail(shp2, hb_d, d["lm_head"], d["U"], d["V"], d["conv_w"], ab_d, o2["pid"], o2["pix"],
-                               o2["score"], ws2, stream=stream)
+            def call2(shp2=shp2, o2=o2, ws2=ws2, dc=dc):
+                df2.draft_tail(shp2, dc["hidden"], dc["lm_head"], dc["U"], dc["V"], dc["conv_w"], dc["anchor"],
+                               o2["pid"], o2["pix"], o2["score"], ws2, stream=stream)
             with torch.cuda.stream(stream):
                 call2()
             torch.cuda.synchronize(dev)
@@ -361,19 +359,29 @@ def run_ours(args, rank, world, local_rank):
             with torch.cuda.graph(g2, stream=stream):
                 call2()
             ms2 = timed(g2.replay, args.steps, 3)
-            z2 = torch.empty_like(hb_d)
-            cv2 = timed(graphed(lambda: df2.conv(shp2, hb_d, d["conv_w"], z2, ws2, stream=stream)), 20, 3)
-            lm2 = timed(graphed(lambda: df2.lmhead_partials(shp2, z2, d["lm_head"], ws2, stream=stream)),
+            z2 = torch.empty_like(dc["hidden"])
+            cv2 = timed(graphed(lambda: df2.conv(shp2, dc["hidden"], dc["conv_w"], z2, ws2, stream=stream)), 20, 3)
+            lm2 = timed(graphed(lambda: df2.lmhead_partials(shp2, z2, dc["lm_head"], ws2, stream=stream)),
                         args.steps, 3)
             us = statistics.mean(ms2) * 1e3
             lmu = statistics.mean(lm2) * 1e3
-            roof = tail_roofline_us(sh, b2 * T, bw, tf)
-            extra[f"B={b2}"] = {
-                "us_per_call": round(us, 2), "blocks_per_s": round(b2 / (us * 1e-6), 1),
-                "tail_roofline_frac": round(roof / us, 4), "lmhead_us": round(lmu, 2),
-                "conv_us": round(statistics.mean(cv2) * 1e3, 2),
-                "lmhead_hbm_gbs": round(lmhead_alg_bytes(sh, b2 * T) / (lmu * 1e-6) / 1e9, 1),
-                "lmhead_tflops": round(2.0 * b2 * T * H * sh.vocab / (lmu * 1e-6) / 1e12, 1)}
+            roof = tail_roofline_us(sh_c, Mc, bw, tf)
+            roof_sus = tail_roofline_us(sh_c, Mc, bw, tf_sus)
+            lm_tflops = 2.0 * Mc * H * sh_c.vocab / (lmu * 1e-6) / 1e12
+            extra[f"B={Bc}"] = {
+                "workload": rc_c.name, "block": Tc, "rows": Mc,
+                "us_per_call": round(us, 2), "blocks_per_s": round(Bc / (us * 1e-6), 1),
+                "tail_roofline_us": round(roof, 1), "tail_roofline_frac": round(roof / us, 4),
+                "tail_roofline_frac_sustained_bf16": round(roof_sus / us, 4),
+                "bound": "tensor" if 2.0 * Mc * H * sh_c.vocab / (tf * 1e12) > sh_c.vocab * H * 2 / (bw * 1e9)
+                else "hbm",
+                "lmhead_us": round(lmu, 2), "conv_us": round(statistics.mean(cv2) * 1e3, 2),
+                "lmhead_hbm_gbs": round(lmhead_alg_bytes(sh_c, Mc) / (lmu * 1e-6) / 1e9, 1),
+                "lmhead_tflops": round(lm_tflops, 1),
+                "lmhead_tensor_frac_burst": round(lm_tflops / tf, 4),
+                "lmhead_tensor_frac_sustained": round(lm_tflops / tf_sus, 4)}
+            del dc, ws2, g2, z2
+            torch.cuda.empty_cache()
 
     if not args.no_extra and world == 1:
         # the same workload with the context gate H(h_t): gate rows contracted in the LM-head
@@ -516,14 +524,46 @@ def oracle_shard_step(rc, inp, shard: int, n_shards: int):
     return O.draft_tail(sub, sh2)
 
 
-def cpu_baseline(rc, inp, n_shards=1):
+def oracle_child(config: int) -> None:
+    """Child process of the CPU baseline: one full block of the workload through the oracle, timed
+    after the inputs are generated; prints the seconds. BLAS threads are fixed by the parent's
+    environment before numpy loads."""
+    from oracle import core as O
+    rc, inp = make_workload(config)
     t0 = time.perf_counter()
-    for s in range(n_shards):
-        oracle_shard_step(rc, inp, s, n_shards)
-    dt = time.perf_counter() - t0
-    return {"value": round(1.0 / dt, 5), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+    O.draft_tail(inp, rc.shape)
+    print(json.dumps({"seconds": time.perf_counter() - t0}), flush=True)
+
+
+def oracle_block_seconds(config: int, threads: int) -> float:
+    env = dict(os.environ)
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[k] = str(threads)
+    out = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-child", str(config)], env=env,
+                         capture_output=True, text=True, check=True)
+    return float(json.loads(out.stdout.strip().splitlines()[-1])["seconds"])
+
+
+def cpu_machine() -> str:
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part", "hardware")):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
+def cpu_baseline(rc, config: int):
+    """The oracle on the host: one full block single-threaded (the plain, slow CPU implementation,
+    one BLAS thread) and with BLAS on every host core."""
+    cores = os.cpu_count() or 1
+    t1 = oracle_block_seconds(config, 1)
+    tn = oracle_block_seconds(config, cores)
+    return {"value": round(1.0 / t1, 5), "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"one full block of {rc.name} (all {rc.shape.block} slots, whole vocabulary) through the "
-                      f"numpy float64 oracle: {dt:.1f} s; OpenBLAS threads = host cores"}
+                      f"numpy float64 oracle, one thread: {t1:.1f} s; CPU: {cpu_machine()}",
+            "all_cores": {"value": round(1.0 / tn, 5), "cores": cores, "seconds": round(tn, 2)}}
 
 
 def run_reference(args, rank, world):
@@ -564,6 +604,9 @@ def run_reference(args, rank, world):
 
 def main():
     args = parse()
+    if args.oracle_child is not None:
+        oracle_child(args.oracle_child)
+        return
     if args.kernel:
         run_kernel_case(args)
         return
@@ -581,7 +624,8 @@ def main():
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     line, rc, inp = run_ours(args, rank, world, local_rank)
     if rank == 0 and world == 1 and not args.no_extra:
-        line["cpu_baseline"] = cpu_baseline(rc, inp)
+        del inp
+        line["cpu_baseline"] = cpu_baseline(rc, args.config)
     if world > 1:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()

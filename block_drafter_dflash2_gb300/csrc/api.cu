@@ -98,6 +98,7 @@ struct Plan {
   size_t esz;
   int n_rc;
   int a_tail_rows;  // rows of the last 128-row chunk, rounded up to 8
+  bool lm_pair;     // LM head on CTA pairs (more than one row chunk)
   int lm_parts;
   int conv_parts;
   bool chain;                // all conv layers in one cooperative launch (small M)
@@ -149,14 +150,23 @@ dflash2_status_t make_plan(const dflash2_shape_t* s, Plan& p) {
     p.n_rc = (p.M + 127) / 128;
     p.a_tail_rows = (p.M % 128 == 0) ? 128 : ((p.M % 128 + 7) / 8) * 8;
     const int per = sms / p.n_rc > 0 ? sms / p.n_rc : 1;
-    p.lm_parts = per < v_units ? per : v_units;
-    // The row-chunk CTAs of a column range each load the whole weight tile; the second read
-    // of a tile mostly hits L2.
+    // More than one row chunk: the LM head runs on CTA pairs, two row chunks per pair sharing
+    // each weight tile (each SM loads half of it), so a column range has one pair per two chunks
+    p.lm_pair = p.n_rc >= 2;
+    if (p.lm_pair) {
+      const int n_prc = (p.n_rc + 1) / 2;
+      const int per_pair = sms / (2 * n_prc) > 0 ? sms / (2 * n_prc) : 1;
+      const int pair_units = (p.V + 31) / 32;
+      p.lm_parts = per_pair < pair_units ? per_pair : pair_units;
+    } else {
+      p.lm_parts = per < v_units ? per : v_units;
+    }
     p.conv_parts = per < p_units ? per : p_units;
     p.split = p.M > kChainMaxRows && p.NL > 0 && df::conv_splitk_plan(p.M, p.H, p.NL, sms, &p.split_plan);
     p.chain = !p.split && df::conv_chain_plan(p.M, p.H, sms, &p.chain_plan);
   } else {
     p.n_rc = 1;
+    p.lm_pair = false;
     p.a_tail_rows = 0;
     p.lm_parts = sms < v_units ? sms : v_units;
     p.conv_parts = 0;
@@ -254,7 +264,7 @@ dflash2_status_t run_conv(const Plan& p, const void* x, const void* conv_w, void
       if (!encode_bf16_2d(&ma, cur, p.H, p.M, 128) || !encode_bf16_2d(&mat, cur, p.H, p.M, p.a_tail_rows) ||
           !encode_bf16_2d(&mb128, wl, p.H, p.P, 128) || !encode_bf16_2d(&mb16, wl, p.H, p.P, 16))
         return DFLASH2_ERR_CUDA;
-      TcGemmArgs a{p.M, p.H, p.P, p.n_rc, p.conv_parts, p.a_tail_rows, 8, w.err};
+      TcGemmArgs a{p.M, p.H, p.P, p.n_rc, p.conv_parts, p.a_tail_rows, 8, 0, w.err};
       if (df::launch_conv_layer_bf16(ma, mat, mb128, mb16, a, cur, out, p.T, p.raw ? 1 : 0, s) != cudaSuccess)
         return DFLASH2_ERR_CUDA;
     } else {
@@ -274,12 +284,13 @@ dflash2_status_t run_partials(const Plan& p, const void* rows, const void* lm_he
   // 256-column tiles once the row tile is not small: each stage's row-tile box is then shared
   // by twice the weight columns (the copy engine issues box rows at a fixed rate; at 8 rows the
   // stream is HBM-bound either way), and several row chunks re-read each row tile half as often
-  TcGemmArgs a{p.M, p.H, p.V, p.n_rc, p.lm_parts, p.a_tail_rows, (p.n_rc > 1 || p.M >= 32) ? 16 : 8, w.err};
+  TcGemmArgs a{p.M, p.H, p.V, p.n_rc, p.lm_parts, p.a_tail_rows, (p.n_rc > 1 || p.M >= 32) ? 16 : 8,
+               p.lm_pair ? 1 : 0, w.err};
   if (gate_w) {
     // the gate rows are one more partition: the last CTA's (the vocabulary keeps the others)
     if (!gate_out) return DFLASH2_ERR_INVALID_ARGUMENT;
     a.parts = gated_parts(p);
-    a.gate_base = (p.V + 15) / 16 * 16;
+    a.gate_base = (p.V + 31) / 32 * 32;
     a.gate_cols = p.R;
   }
   if (p.bf16) {

@@ -7,10 +7,38 @@
 namespace df {
 
 namespace {
+// CTA pairs (more than one row chunk): clusters of two, one per (row-chunk pair, column range).
+// The launch waits for the previous kernel as usual.
+template <class Epi>
+cudaError_t launch_gemm_pair(const CUtensorMap& a, const CUtensorMap& a_tail, const CUtensorMap& b128,
+                             const CUtensorMap& b16, const CUtensorMap& g128, const CUtensorMap& g16,
+                             const TcGemmArgs& args, const typename Epi::Params& ep, cudaStream_t s) {
+  if (!args.pair || args.tile_units % 2 != 0 || args.gate_base % 32 != 0) return cudaErrorInvalidValue;
+  static unsigned char smem_done[64];
+  cudaError_t e = smem_opt_in(reinterpret_cast<const void*>(tc_gemm_pair_kernel<Epi>), smem_done);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2 * ((args.n_rc + 1) / 2) * args.parts));
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = kPairSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<Epi>, a, a_tail, b128, b16, g128, g16, args, ep);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 template <class Epi>
 cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& a_tail, const CUtensorMap& b128,
                         const CUtensorMap& b16, const CUtensorMap& g128, const CUtensorMap& g16,
                         const TcGemmArgs& args, const typename Epi::Params& ep, cudaStream_t s) {
+  if (args.pair) return cudaErrorInvalidValue;
   static unsigned char smem_done[64];
   cudaError_t e = smem_opt_in(reinterpret_cast<const void*>(tc_gemm_kernel<Epi>), smem_done);
   if (e != cudaSuccess) return e;
@@ -44,6 +72,7 @@ cudaError_t launch_lmhead_topk_bf16(const CUtensorMap& a, const CUtensorMap& a_t
                              args.n_total != vocab || args.parts < 2))
     return cudaErrorInvalidValue;
   EpiTopK::Params ep{part_val, part_id, part_ms, args.M, vocab, gate_out, args.gate_base, args.gate_cols};
+  if (args.pair) return launch_gemm_pair<EpiTopK>(a, a_tail, b128, b16, g128, g16, args, ep, s);
   return launch_gemm<EpiTopK>(a, a_tail, b128, b16, g128, g16, args, ep, s);
 }
 

@@ -105,6 +105,78 @@ DF_DEV void tma_load_2d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, i
       : "memory");
 }
 
+// ---------------------------------------------------------------- clusters and distributed shared memory
+
+DF_DEV uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// The shared::cluster address of the variable at shared::cta address `addr` in CTA `rank` of
+// this cluster.
+DF_DEV uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+// One arrival, with release semantics at cluster scope, on the mbarrier at shared::cluster
+// address `addr` (possibly in another CTA of the cluster).
+DF_DEV void mbar_arrive_remote(uint32_t addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+
+DF_DEV bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait, with acquire semantics at cluster scope, for a phase that other CTAs of the
+// cluster complete (their writes before the arrivals are then visible). As mbar_wait otherwise.
+DF_DEV bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, int32_t* err, volatile int* abort) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (abort && *abort) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        flag_error(err, DFLASH2_DEVERR_WAIT_TIMEOUT);
+        if (abort) *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// All threads of all CTAs of the cluster (hardware barrier; every thread must reach it).
+DF_DEV void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Named barrier among `count` threads (whole warps, each converged) of this CTA that also returns,
+// to every participant, the OR of their `pred`s: a decision all of them take the same way.
+DF_DEV bool named_barrier_or(uint32_t id, uint32_t count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
 // ---------------------------------------------------------------- tcgen05
 
 DF_DEV void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
@@ -137,6 +209,53 @@ DF_DEV void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_u32(bar))
                : "memory");
+}
+
+// ---- CTA pairs (cta_group::2): two CTAs of a cluster (ranks 2k, 2k+1) run one MMA of M = 256
+// rows, each holding 128 rows of A and half of the N columns of B in shared memory at the same
+// offsets, and 128 rows of the accumulator in its own TMEM. The TMEM allocation is collective:
+// one warp of each CTA of the pair executes it, and both receive the same address.
+
+DF_DEV void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+
+DF_DEV void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+DF_DEV void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Issued by one thread of the even CTA: D (each CTA's TMEM at d_tmem) (+)= A B^T over both CTAs.
+DF_DEV void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on the mbarrier at shared::cluster address `bar_cluster` (this CTA's or the peer's) once
+// every pair MMA issued so far by this thread has completed.
+DF_DEV void umma_commit_pair(uint32_t bar_cluster) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar_cluster)
+               : "memory");
+}
+
+// 2-D tiled load into this CTA's shared memory whose completion (transaction bytes) is signalled
+// on the mbarrier at shared::cluster address `bar_cluster`, which may be the peer CTA's.
+DF_DEV void tma_load_2d_pair(void* smem_dst, const CUtensorMap* map, uint32_t bar_cluster, int32_t c0, int32_t c1,
+                             uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2.L2::cache_hint"
+      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "l"(policy)
+      : "memory");
 }
 
 // Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, shape M x N.

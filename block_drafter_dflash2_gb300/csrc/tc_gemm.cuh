@@ -278,6 +278,267 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
+// CTA-pair form, for more than one row chunk. The two CTAs of a cluster (ranks 0 and 1) take row
+// chunks 2k and 2k + 1 of the same column range and run each tile as one MMA of M = 256 rows
+// (tcgen05 cta_group::2, issued by rank 0): each CTA loads its own 128 A rows and half of the
+// tile's columns of B (rank 0 the first half), so each weight byte crosses into one SM, not two,
+// and a stage is 32 KB per SM instead of 48 (7 stages in the ring instead of 4). Each CTA's TMEM
+// holds its 128 rows of the accumulator over the tile's full width, so the epilogue is the same
+// thread-per-row reduction as above. Both CTAs' copies of a stage complete on rank 0's full
+// barrier; rank 0's MMA thread commits every stage to the empty barriers of both CTAs and every
+// tile to both CTAs' TMEM-full barriers; each CTA's epilogue releases the accumulator with one
+// arrival on rank 0's TMEM-empty barrier. Ranges are balanced in units of 32 columns so every
+// tile splits evenly (a range's last tile may run up to 16 columns past the vocabulary or the gate
+// matrix: those rows are outside the tensor maps, read as zeros and never ranked or stored).
+// ---------------------------------------------------------------------------
+constexpr int kPairRingBytes = 224 * 1024;
+constexpr int kPairSmemBytes = 1024 /*align*/ + kBarrierBytes + kPairRingBytes;
+
+DF_DEV TileRange tile_range_pair(const TcGemmArgs& a, int part) {
+  TileRange r;
+  if (is_gate_part(a, part)) {
+    r.u0 = a.gate_base / 16;
+    r.u1 = r.u0 + 2 * ((a.gate_cols + 31) / 32);
+    r.col_end = a.gate_base + a.gate_cols;
+  } else {
+    const int pairs = (a.n_total + 31) / 32;
+    const int vparts = a.gate_cols > 0 ? a.parts - 1 : a.parts;
+    r.u0 = 2 * (int)((int64_t)part * pairs / vparts);
+    r.u1 = 2 * (int)((int64_t)(part + 1) * pairs / vparts);
+    r.col_end = min(r.u1 * 16, a.n_total);
+  }
+  r.num_tiles = (r.u1 - r.u0 + a.tile_units - 1) / a.tile_units;
+  return r;
+}
+
+template <class Epi>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_a_tail,
+                        const __grid_constant__ CUtensorMap map_b128, const __grid_constant__ CUtensorMap map_b16,
+                        const __grid_constant__ CUtensorMap map_g128, const __grid_constant__ CUtensorMap map_g16,
+                        const TcGemmArgs args, const typename Epi::Params ep) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(base);
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* tfull = empty + kMaxStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint8_t* ring = base + kBarrierBytes;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs; 1: its peer
+  const int n_prc = (args.n_rc + 1) / 2;
+  const int cl = (int)(blockIdx.x >> 1);
+  const int prc = cl % n_prc, part = cl / n_prc;
+  if (part >= args.parts) return;  // both CTAs of the pair (same cluster) leave together
+  const int rc = 2 * prc + (int)rank;       // this CTA's row chunk (>= n_rc: none)
+  const int peer_rc = 2 * prc + (int)(rank ^ 1u);
+  const TileRange tr = tile_range_pair(args, part);
+  const int kblocks = args.K / kBK;
+  const int TU = args.tile_units;  // even: tiles are whole pairs of 16-column units
+  // identical stage layout in both CTAs: 128 A rows, then the widest tile's half of B
+  const uint32_t b_off = (uint32_t)kBM * kBK * 2;
+  const int half_max = min(TU, tr.u1 - tr.u0) * 8;
+  const uint32_t stride = (b_off + (uint32_t)half_max * kBK * 2 + 1023u) & ~1023u;
+  const int stages = min(kMaxStages, (int)(kPairRingBytes / stride));
+  auto a_rows = [&](int chunk) {
+    return chunk >= args.n_rc ? 0 : (chunk == args.n_rc - 1 ? args.a_tail_rows : kBM);
+  };
+  const uint32_t own_a = (uint32_t)a_rows(rc) * kBK * 2;
+  const uint32_t peer_a = (uint32_t)a_rows(peer_rc) * kBK * 2;
+  const uint32_t tmem_cols = (uint32_t)(2 * TU * 16);
+
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&full[s], 1);   // rank 0's producer arrives with both CTAs' bytes
+      mbar_init(&empty[s], 1);  // rank 0's MMA commit
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 2);  // one arrival per CTA of the pair
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, tmem_cols);
+    tmem_relinquish_pair();
+  }
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(rc == args.n_rc - 1 ? &map_a_tail : &map_a);
+    tma_prefetch_desc(&map_b128);
+    tma_prefetch_desc(&map_b16);
+    if (is_gate_part(args, part)) {
+      tma_prefetch_desc(&map_g16);
+      if (args.gate_cols >= 128) tma_prefetch_desc(&map_g128);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_barrier();  // both CTAs' barriers exist before either signals the other's
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint32_t lead_full = mapa_shared(smem_u32(full), 0);      // + 8 s: rank 0's full[s]
+  const uint32_t peer_empty = mapa_shared(smem_u32(empty), 1);    // + 8 s: rank 1's empty[s]
+  const uint32_t peer_tfull = mapa_shared(smem_u32(tfull), 1);    // + 8 b
+  const uint32_t lead_tempty = mapa_shared(smem_u32(tempty), 0);  // + 8 b
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer (both CTAs)
+      const uint64_t pol_a = l2_policy_evict_last();
+      const uint64_t pol_b = l2_policy_evict_first();
+      const bool tail_chunk = rc == args.n_rc - 1;
+      const CUtensorMap* ma = tail_chunk ? &map_a_tail : &map_a;
+      const bool gate_part = is_gate_part(args, part);
+      const CUtensorMap* mb128 = gate_part ? &map_g128 : &map_b128;
+      const CUtensorMap* mb16 = gate_part ? &map_g16 : &map_b16;
+      const int row0 = gate_part ? args.gate_base : 0;
+      pdl_wait();
+      int stage = 0;
+      uint32_t phase = 0;
+      uint64_t issued = 0, issued_phase = 0;
+      bool ok = true;
+      for (int t = 0; t < tr.num_tiles && ok; ++t) {
+        const int cu0 = tr.u0 + t * TU;
+        const int nu = min(TU, tr.u1 - cu0);  // even
+        const int half = nu * 8;              // columns of B this CTA loads
+        const int my_n0 = cu0 * 16 + (int)rank * half;
+        const uint32_t bytes = own_a + peer_a + 2u * (uint32_t)half * kBK * 2;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, args.err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = ring + (size_t)stage * stride;
+          uint8_t* sb = sa + b_off;
+          const uint32_t fb = lead_full + 8u * (uint32_t)stage;
+          if (rank == 0) mbar_arrive_expect_tx(&full[stage], bytes);
+          if (own_a) tma_load_2d_pair(sa, ma, fb, kb * kBK, rc * kBM, pol_a);
+          if (half == 128) {
+            tma_load_2d_pair(sb, mb128, fb, kb * kBK, my_n0 - row0, pol_b);
+          } else {
+            for (int j = 0; j < half / 16; ++j)
+              tma_load_2d_pair(sb + j * 16 * kBK * 2, mb16, fb, kb * kBK, my_n0 - row0 + 16 * j, pol_b);
+          }
+          issued |= 1ull << stage;
+          issued_phase = (issued_phase & ~(1ull << stage)) | ((uint64_t)phase << stage);
+          if (++stage == stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // Aborted. Rank 0 lets the stages it issued land (their bytes include the peer's); the
+        // peer cannot see its copies complete (they signal rank 0), so it waits a fixed 50 us.
+        if (rank == 0) {
+          for (int s = 0; s < stages; ++s)
+            if ((issued & (1ull << s)) && !mbar_wait(&full[s], (uint32_t)(issued_phase >> s) & 1u, args.err, nullptr))
+              break;
+        } else {
+          const uint64_t t0 = globaltimer_ns();
+          while (globaltimer_ns() - t0 < 50000ull) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ---------------- MMA issuer (rank 0 only)
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = 0; t < tr.num_tiles && ok; ++t) {
+        const int acc = t & 1;
+        const uint32_t acc_phase = (uint32_t)(t >> 1) & 1u;
+        const int nu = min(TU, tr.u1 - (tr.u0 + t * TU));
+        const uint32_t idesc = idesc_bf16_f32(2 * kBM, nu * 16);
+        if (!mbar_wait_cluster(&tempty[acc], acc_phase ^ 1u, args.err, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * TU * 16);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&full[stage], phase, args.err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(ring + (size_t)stage * stride);
+          const uint64_t da = sdesc_k_sw128(sa);
+          const uint64_t db = sdesc_k_sw128(sa + b_off);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            umma_bf16_pair(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+          umma_commit_pair(smem_u32(&empty[stage]));
+          umma_commit_pair(peer_empty + 8u * (uint32_t)stage);
+          if (++stage == stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) {
+          umma_commit_pair(smem_u32(&tfull[acc]));
+          umma_commit_pair(peer_tfull + 8u * (uint32_t)acc);
+        }
+      }
+      // no MMA may still be running (in either CTA) when the pair frees TMEM
+      umma_commit_pair(smem_u32(drain));
+      mbar_wait(drain, 0, args.err, nullptr);
+    }
+  } else {
+    // ---------------- epilogue (both CTAs): thread = TMEM lane = row of this CTA's chunk
+    const int q = warp & 3;
+    const int row = rc * kBM + q * 32 + lane;
+    const bool row_ok = rc < args.n_rc && row < args.M;
+    const bool warp_rows = rc < args.n_rc && rc * kBM + q * 32 < args.M;
+    typename Epi::State st;
+    Epi::init(st);
+    for (int t = 0; t < tr.num_tiles; ++t) {
+      const int acc = t & 1;
+      const uint32_t acc_phase = (uint32_t)(t >> 1) & 1u;
+      const int n0 = (tr.u0 + t * TU) * 16;
+      const int nt = min(TU, tr.u1 - (tr.u0 + t * TU)) * 16;
+      // lane 0 waits and its warp follows (the TMEM loads are warp-wide); the four warps then
+      // agree at the barrier whether any of them gave up
+      int ready = 0;
+      if (lane == 0) ready = mbar_wait(&tfull[acc], acc_phase, args.err, abort_flag) ? 1 : 0;
+      ready = __shfl_sync(0xffffffffu, ready, 0);
+      if (ready) {
+        tc_fence_after();
+        if (warp_rows) {
+          for (int c = 0; c < nt; c += 32) {
+            float v[32];
+            tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * TU * 16 + c), v);
+            Epi::consume(st, ep, v, row, row_ok, n0 + c, min(32, nt - c), tr.col_end);
+          }
+        }
+        tc_fence_before();
+      }
+      __syncwarp();
+      if (named_barrier_or(1, 128, !ready)) break;  // the accumulator was read by all four warps
+      if (warp == 2 && lane == 0) {
+        if (rank == 0) mbar_arrive(&tempty[acc]);
+        else mbar_arrive_remote(lead_tempty + 8u * (uint32_t)acc);
+      }
+    }
+    if (!*abort_flag) Epi::finish(st, ep, row, row_ok, part);
+  }
+
+  __syncthreads();
+  cluster_barrier();  // rank 0 has drained its MMAs, which write both CTAs' TMEM and read both rings
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, tmem_cols);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Epilogue 1: running top-16 (logit desc, id asc) and online log-sum-exp per row.
 // Each thread sees its row's columns in increasing id order, so inserting only values
 // strictly above the current 16th keeps equal logits in id order.
