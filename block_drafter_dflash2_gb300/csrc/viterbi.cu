@@ -126,8 +126,8 @@ __device__ __forceinline__ void store_tau(const float (&acc)[2][4], float (&tau)
 // staged column). Per 64-column chunk each lane forms V g in fp32 for its pieces and splits it
 // into hi = bf16(V g) and lo = bf16(V g - hi); hi is written over the staged V rows and
 // contracted, then lo, so no extra shared memory is needed. The staged V rows are consumed.
-__device__ __forceinline__ void tile_mma_gated(const __nv_bfloat16* stA, __nv_bfloat16* stB, int rc,
-                                               const float* __restrict__ g, float (&acc)[2][4]) {
+__device__ __forceinline__ void tile_mma_gated(const __nv_bfloat16* stA, __nv_bfloat16* stB, int rc, const float* g,
+                                               float (&acc)[2][4]) {
   const int lane = threadIdx.x & 31;
   for (int c0 = 0; c0 < rc; c0 += 64) {
     const int cw = min(64, rc - c0);  // a multiple of 16
@@ -139,8 +139,8 @@ __device__ __forceinline__ void tile_mma_gated(const __nv_bfloat16* stA, __nv_bf
       if (v < kKP * vpr) {
         const int row = v / vpr, cv = v % vpr;
         uint4* p = reinterpret_cast<uint4*>(stB + row * kRowPad + c0 + cv * 8);
-        const float4 g0 = __ldg(reinterpret_cast<const float4*>(g + c0 + cv * 8));
-        const float4 g1 = __ldg(reinterpret_cast<const float4*>(g + c0 + cv * 8 + 4));
+        const float4 g0 = *reinterpret_cast<const float4*>(g + c0 + cv * 8);  // global or staged in shared memory
+        const float4 g1 = *reinterpret_cast<const float4*>(g + c0 + cv * 8 + 4);
         const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
         uint4 x = *p;
         __nv_bfloat162* x2 = reinterpret_cast<__nv_bfloat162*>(&x);
@@ -488,12 +488,13 @@ __host__ __device__ inline size_t merge_stage_bytes(int parts) {
 }
 
 // Per-warp region of the fused kernel: the merge staging of one row, later the gathered
-// V rows of its slot and the U rows that feed the next slot's tile.
+// V rows of its slot, the U rows that feed the next slot's tile and the slot's gate row.
 constexpr size_t kTileStageBytes = (size_t)2 * kKP * kRowPad * sizeof(__nv_bfloat16);
+constexpr size_t kGateStageBytes = (size_t)kRChunk * sizeof(float);
 constexpr size_t kAnchorStageBytes = (size_t)kKP * kRowPad * sizeof(__nv_bfloat16);
 __host__ __device__ inline size_t select_region_stride(int parts) {
   const size_t m = merge_stage_bytes(parts);
-  return m > kTileStageBytes ? m : kTileStageBytes;
+  return m > kTileStageBytes + kGateStageBytes ? m : kTileStageBytes + kGateStageBytes;
 }
 
 template <bool kBf16>
@@ -593,6 +594,11 @@ __global__ void __launch_bounds__(32 * kWarps)
         __nv_bfloat16* stB = reinterpret_cast<__nv_bfloat16*>(region + warp * wstride);
         gather_rows(reinterpret_cast<const __nv_bfloat16*>(Vv), R, sw.ids[t], stB);
         if (t + 1 < T) gather_rows(reinterpret_cast<const __nv_bfloat16*>(Uv), R, sw.ids[t], stB + kKP * kRowPad);
+        if (gate) {  // the slot's gate row, read by the tile's hi / lo split
+          float* gs = reinterpret_cast<float*>(region + warp * wstride + kTileStageBytes);
+          const float* gsrc = gate + ((size_t)b * rows_per_seq + first + t) * R;
+          for (int v = lane; v < R / 4; v += 32) cp_async16(gs + v * 4, gsrc + v * 4);
+        }
         cp_async_commit();
       }
     }
@@ -605,7 +611,7 @@ __global__ void __launch_bounds__(32 * kWarps)
           warp == 0 ? a0 : reinterpret_cast<const __nv_bfloat16*>(region + (warp - 1) * wstride) + kKP * kRowPad;
       __nv_bfloat16* stB = reinterpret_cast<__nv_bfloat16*>(region + warp * wstride);
       float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      if (gate) tile_mma_gated(stA, stB, R, gate + ((size_t)b * rows_per_seq + first + warp) * R, acc);
+      if (gate) tile_mma_gated(stA, stB, R, reinterpret_cast<const float*>(region + warp * wstride + kTileStageBytes), acc);
       else tile_mma(stA, stB, R, acc);
       store_tau(acc, sw.tau[warp]);
     }
