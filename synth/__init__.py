@@ -3,7 +3,10 @@
 Holds none of the draft tail's arithmetic: only the counter-based generator
 (Philox4x32-10, Salmon et al., SC'11), the Box-Muller normals built from it, and
 the input recipes (shapes, scales, RMS normalisation of the hidden rows, planted
-peaks) for the five workloads. The C core is ``synth.c``; this module compiles it
+peaks) for the five workloads. The planted peaks are stored data: the planted tokens'
+lm_head rows are moved by deltas that a committed script computed once from the CPU
+oracle's conv output (``tests/golden/make_planted_rows.py``); this module only draws
+which slots are planted with which token and adds the stored deltas. The C core is ``synth.c``; this module compiles it
 with the host C compiler on first use and loads it with ctypes.
 
 Tensor ids (the second Philox key word) are fixed per tensor so the order in
@@ -164,17 +167,23 @@ class Recipe:
     uv_std: float = 0.05
     conv_std: float = 0.02
     gate_std: float = 0.0  # 0: 1 / sqrt(hidden), so a gate entry of a unit-rms row is about N(0, 1)
-    plant: str = "none"  # 'none', 'all' (every slot, 1 % left unplanted), 'even_seq' (even sequences)
-    plant_beta: float = 0.0
+    plant: str = "none"  # 'none', 'all' (every slot, 1 % left unplanted), 'even_rows' (slots t even)
     anchor_dup_frac: float = 0.0
     name: str = ""
     extra: dict = field(default_factory=dict)
 
 
-# Planting strength for the peaked rows: the planted token's lm_head row, scaled to unit
-# per-element rms, is added with this weight to the slot's N(0,1) hidden row before the
-# RMS normalisation (see make_inputs).
-PLANT_BETA = 5.0
+# Planted peaks: a planted slot's token gets top-1 probability PLANT_MASS at that slot (its
+# logit set to the log-sum-exp of the slot's other logits plus log(PLANT_MASS / (1 - PLANT_MASS)))
+# through a change of that token's lm_head row that leaves the logits of the sequence's other
+# slots unchanged; the deltas are stored per workload under tests/golden.
+PLANT_MASS = 0.85
+PLANT_SKIP = 0.01  # 'all': the share of slots left unplanted
+GOLDEN_DIR = os.path.join(os.path.dirname(_HERE), "tests", "golden")
+
+
+def planted_rows_path(rc: "Recipe") -> str:
+    return os.path.join(GOLDEN_DIR, f"planted_rows_{rc.name}.npz")
 
 
 def recipe(config: int) -> Recipe:
@@ -189,13 +198,13 @@ def recipe(config: int) -> Recipe:
                       name="page_b1_t8_h5120_v248320_k16_r256")
     if config == 3:
         return Recipe(seed=2, shape=Shape(batch=8, block=8, **page), rms_normalise=True,
-                      plant="all", plant_beta=PLANT_BETA, name="page_b8_t8_planted")
+                      plant="all", name="page_b8_t8_planted")
     if config == 4:
         return Recipe(seed=3, shape=Shape(batch=32, block=8, **page), rms_normalise=True,
                       anchor_dup_frac=0.25, name="page_b32_t8_dup_anchors")
     if config == 5:
         return Recipe(seed=4, shape=Shape(batch=64, block=16, **page), rms_normalise=True,
-                      plant="even_seq", plant_beta=PLANT_BETA, name="stress_b64_t16_half_planted")
+                      plant="even_rows", name="stress_b64_t16_half_planted")
     raise ValueError(f"unknown workload {config}")
 
 
@@ -205,13 +214,56 @@ def scaled_recipe(base: Recipe, **shape_overrides) -> Recipe:
     return Recipe(**{**base.__dict__, "shape": sh})
 
 
-def make_inputs(rc: Recipe, with_lm_head: bool = True) -> dict:
+def planted_slots(rc: Recipe) -> np.ndarray:
+    """[B, T] int32: the token planted at each slot, -1 where none. 'all': every slot but about
+    PLANT_SKIP of them; 'even_rows': the slots t even. Tokens are distinct across the workload
+    (a repeat moves to the next free id)."""
+    sh = rc.shape
+    B, T, Vv = sh.batch, sh.block, sh.vocab
+    out = np.full((B, T), -1, dtype=np.int32)
+    if rc.plant == "none":
+        return out
+    ids = uniform_int(rc.seed, TID_PLANT_ID, B * T, Vv).reshape(B, T)
+    on_u = uniform(rc.seed, TID_PLANT_ON, B * T).reshape(B, T)
+    used = set()
+    for b in range(B):
+        for t in range(T):
+            if rc.plant == "all" and on_u[b, t] >= 1.0 - PLANT_SKIP:
+                continue
+            if rc.plant == "even_rows" and t % 2 == 1:
+                continue
+            p = int(ids[b, t])
+            while p in used:
+                p = (p + 1) % Vv
+            used.add(p)
+            out[b, t] = p
+    return out
+
+
+def apply_planted_rows(rc: Recipe, lm_head: np.ndarray, planted: np.ndarray) -> None:
+    """Add the stored deltas to the planted tokens' lm_head rows (bf16, in place): row p becomes
+    bf16(row p + step * code), the codes stored as int8 values -127..127, step the row's step."""
+    path = planted_rows_path(rc)
+    if not os.path.exists(path):
+        raise FileNotFoundError(f"{path} is missing; tests/golden/make_planted_rows.py writes it")
+    st = np.load(path)
+    ids = planted[planted >= 0]
+    if not np.array_equal(st["ids"], ids):
+        raise ValueError(f"{path} was written for other planted slots")
+    q = st["q"].astype(np.float64)
+    rows = bf16_bits_to_f32(lm_head[ids]).astype(np.float64) + q * st["step"][:, None]
+    lm_head[ids] = f64_to_bf16(rows)
+
+
+def make_inputs(rc: Recipe, with_lm_head: bool = True, apply_planting: bool = True) -> dict:
     """Generate every input tensor of one workload.
 
     Returns numpy arrays: ``hidden`` [B,T,H], ``lm_head`` [V,H], ``U``/``V`` [V,R],
     ``conv_w`` [NL,P,H], ``gate_w`` [R,H] (bf16 bit patterns as uint16, or float32 for
     dtype f32) and
     ``anchor`` [B] int32, plus ``planted`` [B,T] int32 (-1 where a slot is not planted).
+    With ``apply_planting`` False the planted tokens' rows are left as drawn (the state the
+    stored deltas were computed from).
     """
     sh = rc.shape
     B, T, H, Vv, R = sh.batch, sh.block, sh.hidden, sh.vocab, sh.rank
@@ -236,27 +288,13 @@ def make_inputs(rc: Recipe, with_lm_head: bool = True) -> dict:
     out["anchor"] = anchor.astype(np.int32)
 
     h = normal(s, TID_HIDDEN, (B, T, H), rc.hidden_std, "f64")
-    planted = np.full((B, T), -1, dtype=np.int32)
-    if rc.plant != "none":
-        if out["lm_head"] is None:
-            raise ValueError("planting needs the lm_head rows")
-        ids = uniform_int(s, TID_PLANT_ID, B * T, Vv).reshape(B, T)
-        on_u = uniform(s, TID_PLANT_ON, B * T).reshape(B, T)
-        for b in range(B):
-            for t in range(T):
-                if rc.plant == "all" and on_u[b, t] >= 0.99:
-                    continue
-                if rc.plant == "even_seq" and b % 2 == 1:
-                    continue
-                p = int(ids[b, t])
-                row = out["lm_head"][p]
-                w = bf16_bits_to_f32(row).astype(np.float64) if kind == "bf16" else row.astype(np.float64)
-                # the planted row's direction, scaled to unit per-element rms, mixed into the slot
-                w = w / np.sqrt(np.mean(w * w))
-                h[b, t] = h[b, t] + rc.plant_beta * w
-                planted[b, t] = p
     if rc.rms_normalise:
         h = h / np.sqrt(np.mean(h * h, axis=-1, keepdims=True) + 1e-6)
     out["hidden"] = f64_to_bf16(h) if kind == "bf16" else h.astype(np.float32)
+    planted = planted_slots(rc)
+    if rc.plant != "none" and apply_planting:
+        if out["lm_head"] is None:
+            raise ValueError("planting needs the lm_head rows")
+        apply_planted_rows(rc, out["lm_head"], planted)
     out["planted"] = planted
     return out

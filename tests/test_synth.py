@@ -86,3 +86,30 @@ def test_conv_comparator_catches_planted_errors():
     chain[0, 0, 0] ^= 1
     with pytest.raises(AssertionError):
         P.check_conv_layers(h, w, "bf16", "softmax", layers, chain, ref_chain=ref)
+
+
+def test_planted_rows_reach_the_stated_peaks():
+    # the B=8 planted workload: the stored deltas move only the planted tokens' rows, and at a few
+    # planted slots (the oracle's own logits over the whole vocabulary) the planted token takes
+    # about 85 % of the mass and tops the slot, while its logit at the sequence's other rows stays
+    # where it was before planting
+    rc = synth.recipe(3)
+    sh = rc.shape
+    planted = synth.planted_slots(rc)
+    assert (planted >= 0).sum() >= 0.95 * planted.size
+    inp = synth.make_inputs(rc)
+    drawn = synth.normal(rc.seed, synth.TID_LM_HEAD, (sh.vocab, sh.hidden), rc.lm_head_std, "bf16")
+    changed = np.nonzero(np.any(inp["lm_head"] != drawn, axis=1))[0]
+    assert set(changed.tolist()) <= set(planted[planted >= 0].tolist())
+    z = O.conv_chain(inp["hidden"], inp["conv_w"], "bf16", 16)
+    for b, t in ((0, 1), (3, 5), (6, 7)):
+        p = int(planted[b, t])
+        assert p >= 0
+        l = O.logits(z[b, t][None], inp["lm_head"])[0].astype(np.float64)
+        lse = l.max() + np.log(np.exp(l - l.max()).sum())
+        assert abs(np.exp(l[p] - lse) - synth.PLANT_MASS) < 0.02
+        assert int(np.argmax(l)) == p
+        others = np.stack([z[b, tt] for tt in range(sh.block) if tt != t])
+        before = O.logits(others, drawn[p:p + 1])[:, 0]
+        after = O.logits(others, inp["lm_head"][p:p + 1])[:, 0]
+        assert np.abs(after.astype(np.float64) - before).max() < 1.0
