@@ -292,6 +292,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // matrix: those rows are outside the tensor maps, read as zeros and never ranked or stored).
 // ---------------------------------------------------------------------------
 constexpr int kPairRingBytes = 224 * 1024;
+constexpr int kPairKps = 2;  // K blocks of 64 per ring stage: fewer, larger stages move more bytes per SM
 constexpr int kPairSmemBytes = 1024 /*align*/ + kBarrierBytes + kPairRingBytes;
 
 DF_DEV TileRange tile_range_pair(const TcGemmArgs& a, int part) {
@@ -340,11 +341,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const TileRange tr = tile_range_pair(args, part);
   const int kblocks = args.K / kBK;
   const int TU = args.tile_units;  // even: tiles are whole pairs of 16-column units
-  // identical stage layout in both CTAs: 128 A rows, then the widest tile's half of B
+  // identical stage layout in both CTAs: kPairKps K blocks, each 128 A rows then the widest
+  // tile's half of B
   const uint32_t b_off = (uint32_t)kBM * kBK * 2;
   const int half_max = min(TU, tr.u1 - tr.u0) * 8;
-  const uint32_t stride = (b_off + (uint32_t)half_max * kBK * 2 + 1023u) & ~1023u;
+  const uint32_t sub = (b_off + (uint32_t)half_max * kBK * 2 + 1023u) & ~1023u;
+  const uint32_t stride = sub * kPairKps;
   const int stages = min(kMaxStages, (int)(kPairRingBytes / stride));
+  const int ksteps = (kblocks + kPairKps - 1) / kPairKps;
   auto a_rows = [&](int chunk) {
     return chunk >= args.n_rc ? 0 : (chunk == args.n_rc - 1 ? args.a_tail_rows : kBM);
   };
@@ -410,22 +414,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int nu = min(TU, tr.u1 - cu0);  // even
         const int half = nu * 8;              // columns of B this CTA loads
         const int my_n0 = cu0 * 16 + (int)rank * half;
-        const uint32_t bytes = own_a + peer_a + 2u * (uint32_t)half * kBK * 2;
-        for (int kb = 0; kb < kblocks; ++kb) {
+        const uint32_t bytes = own_a + peer_a + 2u * (uint32_t)half * kBK * 2;  // per K block
+        for (int ks = 0; ks < ksteps; ++ks) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, args.err, abort_flag)) {
             ok = false;
             break;
           }
-          uint8_t* sa = ring + (size_t)stage * stride;
-          uint8_t* sb = sa + b_off;
+          const int nkb = min(kPairKps, kblocks - ks * kPairKps);
           const uint32_t fb = lead_full + 8u * (uint32_t)stage;
-          if (rank == 0) mbar_arrive_expect_tx(&full[stage], bytes);
-          if (own_a) tma_load_2d_pair(sa, ma, fb, kb * kBK, rc * kBM, pol_a);
-          if (half == 128) {
-            tma_load_2d_pair(sb, mb128, fb, kb * kBK, my_n0 - row0, pol_b);
-          } else {
-            for (int j = 0; j < half / 16; ++j)
-              tma_load_2d_pair(sb + j * 16 * kBK * 2, mb16, fb, kb * kBK, my_n0 - row0 + 16 * j, pol_b);
+          if (rank == 0) mbar_arrive_expect_tx(&full[stage], (uint32_t)nkb * bytes);
+          for (int j = 0; j < nkb; ++j) {
+            const int kb = ks * kPairKps + j;
+            uint8_t* sa = ring + (size_t)stage * stride + (size_t)j * sub;
+            uint8_t* sb = sa + b_off;
+            if (own_a) tma_load_2d_pair(sa, ma, fb, kb * kBK, rc * kBM, pol_a);
+            if (half == 128) {
+              tma_load_2d_pair(sb, mb128, fb, kb * kBK, my_n0 - row0, pol_b);
+            } else {
+              for (int i = 0; i < half / 16; ++i)
+                tma_load_2d_pair(sb + i * 16 * kBK * 2, mb16, fb, kb * kBK, my_n0 - row0 + 16 * i, pol_b);
+            }
           }
           issued |= 1ull << stage;
           issued_phase = (issued_phase & ~(1ull << stage)) | ((uint64_t)phase << stage);
@@ -463,18 +471,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (!mbar_wait_cluster(&tempty[acc], acc_phase ^ 1u, args.err, abort_flag)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * TU * 16);
-        for (int kb = 0; kb < kblocks; ++kb) {
+        for (int ks = 0; ks < ksteps; ++ks) {
           if (!mbar_wait(&full[stage], phase, args.err, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_u32(ring + (size_t)stage * stride);
-          const uint64_t da = sdesc_k_sw128(sa);
-          const uint64_t db = sdesc_k_sw128(sa + b_off);
+          const int nkb = min(kPairKps, kblocks - ks * kPairKps);
+          for (int j = 0; j < nkb; ++j) {
+            const uint32_t sa = smem_u32(ring + (size_t)stage * stride + (size_t)j * sub);
+            const uint64_t da = sdesc_k_sw128(sa);
+            const uint64_t db = sdesc_k_sw128(sa + b_off);
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k)
-            umma_bf16_pair(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+            for (int k = 0; k < kBK / 16; ++k)
+              umma_bf16_pair(d_tmem, da + 2 * k, db + 2 * k, idesc, (ks | j | k) != 0 ? 1u : 0u);
+          }
           umma_commit_pair(smem_u32(&empty[stage]));
           umma_commit_pair(peer_empty + 8u * (uint32_t)stage);
           if (++stage == stages) {

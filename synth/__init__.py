@@ -232,6 +232,8 @@ def planted_slots(rc: Recipe) -> np.ndarray:
                 continue
             if rc.plant == "even_rows" and t % 2 == 1:
                 continue
+            if len(used) >= Vv:
+                raise ValueError(f"more planted slots than the {Vv} vocabulary ids")
             p = int(ids[b, t])
             while p in used:
                 p = (p + 1) % Vv
