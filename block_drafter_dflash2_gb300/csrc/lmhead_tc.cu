@@ -19,7 +19,7 @@ cudaError_t launch_gemm_pair(const CUtensorMap& a, const CUtensorMap& a_tail, co
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(2 * ((args.n_rc + 1) / 2) * args.parts));
-  cfg.blockDim = dim3(kGemmThreads);
+  cfg.blockDim = dim3(kPairThreads);
   cfg.dynamicSmemBytes = kPairSmemBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];

@@ -293,6 +293,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // ---------------------------------------------------------------------------
 constexpr int kPairRingBytes = 224 * 1024;
 constexpr int kPairKps = 2;  // K blocks of 64 per ring stage: fewer, larger stages move more bytes per SM
+constexpr int kPairProducer2 = 6;                 // warp of the second TMA producer
+constexpr int kPairThreads = kGemmThreads + 32;  // the single-CTA roles plus that warp
 constexpr int kPairSmemBytes = 1024 /*align*/ + kBarrierBytes + kPairRingBytes;
 
 DF_DEV TileRange tile_range_pair(const TcGemmArgs& a, int part) {
@@ -313,7 +315,7 @@ DF_DEV TileRange tile_range_pair(const TcGemmArgs& a, int part) {
 }
 
 template <class Epi>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(kPairThreads, 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_a_tail,
                         const __grid_constant__ CUtensorMap map_b128, const __grid_constant__ CUtensorMap map_b16,
                         const __grid_constant__ CUtensorMap map_g128, const __grid_constant__ CUtensorMap map_g16,
@@ -393,9 +395,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t peer_tfull = mapa_shared(smem_u32(tfull), 1);    // + 8 b
   const uint32_t lead_tempty = mapa_shared(smem_u32(tempty), 0);  // + 8 b
 
-  if (warp == 0) {
+  if (warp == 0 || warp == kPairProducer2) {
     if (lane == 0) {
-      // ---------------- TMA producer (both CTAs)
+      // ---------------- TMA producers (both CTAs): warp 0 loads K block 0 of every stage and
+      // posts the stage's bytes; the second producer loads K block 1. Two issuing threads move
+      // more bytes into the SM than one. Its copies may land before the byte count is posted:
+      // the count goes below zero and the phase still waits for the posting arrival.
+      const int j = warp == 0 ? 0 : 1;
       const uint64_t pol_a = l2_policy_evict_last();
       const uint64_t pol_b = l2_policy_evict_first();
       const bool tail_chunk = rc == args.n_rc - 1;
@@ -422,8 +428,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           const int nkb = min(kPairKps, kblocks - ks * kPairKps);
           const uint32_t fb = lead_full + 8u * (uint32_t)stage;
-          if (rank == 0) mbar_arrive_expect_tx(&full[stage], (uint32_t)nkb * bytes);
-          for (int j = 0; j < nkb; ++j) {
+          if (j == 0 && rank == 0) mbar_arrive_expect_tx(&full[stage], (uint32_t)nkb * bytes);
+          if (j < nkb) {
             const int kb = ks * kPairKps + j;
             uint8_t* sa = ring + (size_t)stage * stride + (size_t)j * sub;
             uint8_t* sb = sa + b_off;
@@ -444,9 +450,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
       if (!ok) {
-        // Aborted. Rank 0 lets the stages it issued land (their bytes include the peer's); the
-        // peer cannot see its copies complete (they signal rank 0), so it waits a fixed 50 us.
-        if (rank == 0) {
+        // Aborted. Rank 0's first producer lets the stages it posted land (their bytes include
+        // the peer's and the second producer's; a stage whose other copies were never issued
+        // gives up at the wait's time limit); the others cannot see their copies complete
+        // (they signal rank 0's barrier), so they wait a fixed 50 us.
+        if (rank == 0 && j == 0) {
           for (int s = 0; s < stages; ++s)
             if ((issued & (1ull << s)) && !mbar_wait(&full[s], (uint32_t)(issued_phase >> s) & 1u, args.err, nullptr))
               break;
