@@ -150,6 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       wphase ^= 1u;
       if (tid == 0) w_pending = false;
     }
+    __syncwarp();  // the lanes left the waits at different times; mma.sync wants the warp converged
     const __nv_bfloat16* xa_base = kStageX ? xs : xb;
     const __nv_bfloat16* wb_base = kStageW ? ws : wl;
 

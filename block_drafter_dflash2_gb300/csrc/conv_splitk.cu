@@ -186,7 +186,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // TMEM -> shared memory: the tile's partials as [tap][row] in the ring, which every
       // MMA of the layer has finished reading once tfull completes
       const int q = warp & 3;  // TMEM lane quadrant of this warp
-      if (mbar_wait(tfull, (uint32_t)l & 1u, a.err, stop)) {
+      // lane 0 waits and the warp follows it converged: the TMEM loads are warp-wide
+      // (.sync.aligned) and must not be reached by lanes leaving the wait at different times
+      int ready = 0;
+      if (lane == 0) ready = mbar_wait(tfull, (uint32_t)l & 1u, a.err, stop) ? 1 : 0;
+      ready = __shfl_sync(0xffffffffu, ready, 0);
+      __syncwarp();
+      if (ready) {
         tc_fence_after();
         if (q * 32 < rows) {
           for (int c = 0; c < a.Nt; c += 32) {

@@ -255,7 +255,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t acc_phase = (uint32_t)(t >> 1) & 1u;
       const int n0 = (tr.u0 + t * TU) * 16;
       const int nt = min(TU, tr.u1 - (tr.u0 + t * TU)) * 16;
-      if (!mbar_wait(&tfull[acc], acc_phase, args.err, abort_flag)) break;
+      // lane 0 waits and the warp follows it converged (the TMEM loads are warp-wide)
+      int ready = 0;
+      if (lane == 0) ready = mbar_wait(&tfull[acc], acc_phase, args.err, abort_flag) ? 1 : 0;
+      ready = __shfl_sync(0xffffffffu, ready, 0);
+      __syncwarp();
+      if (!ready) break;
       tc_fence_after();
       if (warp_rows) {
         for (int c = 0; c < nt; c += 32) {
