@@ -378,28 +378,30 @@ __device__ void walk_warp0(SmemWalk& sw, int b, int T, int K, int flags, const S
     else sample_warp0(sw, b, T, K, sa, path_ids, path_idx, score);
   } else if (!greedy) {
     // Viterbi in fp32: delta_0 = lp_0 + tau_0(0, j); delta_t = lp_t + max_i (delta_{t-1}(i) + tau_t(i, j)).
-    // delta(i) is read back from shared memory by every lane (a broadcast), so the inner
-    // loop has no shuffle latency in it.
-    __shared__ float dsh[kKP];
+    // Each step, lane j loads its column of tau_t into registers and receives delta(i) by
+    // shuffles, so the max over i runs on registers (lowest i on ties: strict > in i order).
     float delta = live ? sw.lp[0][j] + sw.tau[0][0][j] : -INFINITY;
+    const int jc = j & (kKP - 1);  // lanes past the candidates read a valid column, unused
     for (int t = 1; t < T; ++t) {
-      if (lane < kKP) dsh[lane] = delta;
-      __syncwarp();
-      if (live) {
-        float best = dsh[0] + sw.tau[t][0][j];
-        int arg = 0;
-        for (int i = 1; i < K; ++i) {
-          const float v = dsh[i] + sw.tau[t][i][j];
-          if (v > best) {
-            best = v;
-            arg = i;
-          }
+      float tc[kKP];
+#pragma unroll
+      for (int i = 0; i < kKP; ++i) tc[i] = sw.tau[t][i][jc];
+      float best = __shfl_sync(0xffffffffu, delta, 0) + tc[0];
+      int arg = 0;
+#pragma unroll
+      for (int i = 1; i < kKP; ++i) {
+        const float v = __shfl_sync(0xffffffffu, delta, i) + tc[i];
+        if (i < K && v > best) {
+          best = v;
+          arg = i;
         }
+      }
+      if (live) {
         delta = sw.lp[t][j] + best;
         sw.bp[t][j] = (int8_t)arg;
       }
-      __syncwarp();
     }
+    __syncwarp();
     // arg-max over lanes, lowest index on ties
     float bv = delta;
     int bj = live ? j : 0x7fffffff;
@@ -425,26 +427,30 @@ __device__ void walk_warp0(SmemWalk& sw, int b, int T, int K, int flags, const S
   } else {
     // Greedy: j_t = argmax_j (lp_t(j) + tau_t(j_{t-1}, j)); the score follows the Viterbi
     // recursion's order on the chosen path: delta_t = lp_t(j_t) + (delta_{t-1} + tau_t(j_{t-1}, j_t)).
-    if (lane == 0) {
-      float delta = 0.f;
-      int pj = 0;
-      for (int t = 0; t < T; ++t) {
-        int bj = 0;
-        float bv = 0.f;
-        for (int c = 0; c < K; ++c) {
-          const float v = sw.lp[t][c] + sw.tau[t][t == 0 ? 0 : pj][c];
-          if (c == 0 || v > bv) {
-            bv = v;
-            bj = c;
-          }
+    // Lane c evaluates candidate c and a shuffle arg-max picks the best, lowest index on ties.
+    float delta = 0.f;
+    int pj = 0;
+    for (int t = 0; t < T; ++t) {
+      const int row = t == 0 ? 0 : pj;
+      float bv = live ? sw.lp[t][j] + sw.tau[t][row][j] : -INFINITY;
+      int bj = live ? j : 0x7fffffff;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oj = __shfl_xor_sync(0xffffffffu, bj, o);
+        if (oj < 0x7fffffff && (bj == 0x7fffffff || ov > bv || (ov == bv && oj < bj))) {
+          bv = ov;
+          bj = oj;
         }
-        delta = (t == 0) ? sw.lp[0][bj] + sw.tau[0][0][bj] : sw.lp[t][bj] + (delta + sw.tau[t][pj][bj]);
+      }
+      delta = (t == 0) ? sw.lp[0][bj] + sw.tau[0][0][bj] : sw.lp[t][bj] + (delta + sw.tau[t][pj][bj]);
+      if (lane == 0) {
         path_idx[(size_t)b * T + t] = bj;
         path_ids[(size_t)b * T + t] = sw.ids[t][bj];
-        pj = bj;
       }
-      score[b] = (flags & kWalkFlagScoreLogits) ? delta + lse_sum(sw, T) : delta;
+      pj = bj;
     }
+    if (lane == 0) score[b] = (flags & kWalkFlagScoreLogits) ? delta + lse_sum(sw, T) : delta;
   }
 }
 
