@@ -70,10 +70,15 @@ __global__ void __launch_bounds__(kThreads)
   if (warp != 0) return;
   const float lse = lse_s;
 
-  warp_merge_lists(sv, si, head, parts, K, [&](int k, int32_t id, float v) {
+  int32_t id;
+  float v;
+  bool ok;
+  warp_merge_lists(sv, si, head, parts, K, id, v, ok);
+  const int k = threadIdx.x & 31;
+  if (ok) {
     cand_ids[(size_t)row * K + k] = id;
     cand_lp[(size_t)row * K + k] = v - lse;
-  });
+  }
 }
 }  // namespace
 

@@ -34,79 +34,107 @@ __device__ __forceinline__ void cp_async8(void* smem_dst, const void* gmem_src) 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
+// Inverse of order_key.
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
 // One warp merges `parts` sorted lists of 16 (sv/si: [parts][16] in shared memory, head:
-// [parts] zeroed) into the K best (logit desc, id asc). Lane l owns the lists p = l (mod 32)
-// and keeps its best head; a round is a redux.sync max over the order key, a redux.sync min
-// over the ids of the lanes holding that key (ids are unique across lists), and a ballot for
-// the lowest such lane, which emits its head and advances that list. emit(k, id, logit) is
-// called by the winning lane. Up to kMergeCache lists per lane (32 * kMergeCache partitions)
-// the heads live in registers, so a round reads shared memory once (the winner's next entry);
-// beyond that the winner rescans its lists' heads in shared memory.
+// [parts] zeroed) into the K best (logit desc, id asc); lane k < K receives the k-th in
+// (out_id, out_v) with out_ok set. Lane l owns the lists p = l (mod 32) and keeps its best head.
+// A round is a redux.sync max over the order keys of the lanes' heads and, only when several
+// lanes hold that key, a redux.sync min over their ids (ids are unique across lists); the lowest
+// such lane wins, and every lane learns the round's value from the key and its id by a shuffle.
+// Up to kMergeCache lists per lane the heads are kept in registers as 64-bit keys
+// (order key << 32 | ~id: larger is better, 0 = list exhausted), every lane runs the same
+// branch-free advance and tree pick (only the winner's state changes), so a round reads shared
+// memory once; beyond that the winner rescans its lists' heads in shared memory.
 constexpr int kMergeCache = 8;
 
-template <class Emit>
-__device__ __forceinline__ void warp_merge_lists(const float* sv, const int32_t* si, uint8_t* head, int parts,
-                                                 int K, Emit emit) {
+__device__ __forceinline__ uint64_t entry_key(float v, int32_t id) {
+  return ((uint64_t)order_key(v) << 32) | (uint32_t)(~id);
+}
+
+__device__ __forceinline__ void warp_merge_lists(const float* sv, const int32_t* si, uint8_t* head, int parts, int K,
+                                                 int32_t& out_id, float& out_v, bool& out_ok) {
   const int lane = threadIdx.x & 31;
-  float bv = -INFINITY;
-  int32_t bid = 0x7fffffff;
-  int bp = -1;  // the lane's best list (-1: none left)
-  auto round = [&](auto&& advance) {
-    for (int k = 0; k < K; ++k) {
-      const uint32_t key = bp >= 0 ? order_key(bv) : 0u;
-      const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
-      const bool tied = key == kmax && bp >= 0;
-      const uint32_t wid = __reduce_min_sync(0xffffffffu, tied ? (uint32_t)bid : 0xffffffffu);
-      const uint32_t win = __ballot_sync(0xffffffffu, tied && (uint32_t)bid == wid);
-      if (lane == __ffs(win) - 1) {
-        emit(k, bid, bv);
-        advance();
-      }
-      __syncwarp();
-    }
-  };
+  out_ok = false;
+  out_id = 0;
+  out_v = -INFINITY;
   if (parts <= 32 * kMergeCache) {
-    // heads in registers: hv/hid the head entry of list lane + 32 m, hh its position (16: none)
-    float hv[kMergeCache];
-    int32_t hid[kMergeCache];
-    int hh[kMergeCache];
+    uint64_t hk[kMergeCache];  // head key of list lane + 32 m (0: none left)
+    int hh[kMergeCache];       // its position in the list
 #pragma unroll
     for (int m = 0; m < kMergeCache; ++m) {
       const int p = lane + 32 * m;
       const bool has = p < parts;
-      hh[m] = has ? 0 : 16;
-      hv[m] = has ? sv[p * 16] : -INFINITY;
-      hid[m] = has ? si[p * 16] : 0x7fffffff;
+      hh[m] = 0;
+      const float v0 = sv[has ? p * 16 : 0];
+      const int32_t i0 = si[has ? p * 16 : 0];
+      hk[m] = has ? entry_key(v0, i0) : 0ull;
     }
-    auto pick = [&]() {  // the best head over the lane's lists, in list order (as a rescan would)
-      bv = -INFINITY;
-      bid = 0x7fffffff;
-      bp = -1;
+    uint64_t best = 0;
+    int bm = 0;
+    auto pick = [&]() {  // the largest key; the lower list on equal keys
+      uint64_t k[kMergeCache];
+      int mi[kMergeCache];
 #pragma unroll
       for (int m = 0; m < kMergeCache; ++m) {
-        if (hh[m] < 16 && (bp < 0 || better(hv[m], hid[m], bv, bid))) {
-          bv = hv[m];
-          bid = hid[m];
-          bp = m;
+        k[m] = hk[m];
+        mi[m] = m;
+      }
+#pragma unroll
+      for (int w = 1; w < kMergeCache; w *= 2) {
+#pragma unroll
+        for (int a = 0; a < kMergeCache; a += 2 * w) {
+          const bool gt = k[a + w] > k[a];
+          k[a] = gt ? k[a + w] : k[a];
+          mi[a] = gt ? mi[a + w] : mi[a];
         }
       }
+      best = k[0];
+      bm = mi[0];
     };
     pick();
-    round([&]() {
+    for (int k = 0; k < K; ++k) {
+      const uint32_t key = (uint32_t)(best >> 32);
+      const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
+      const bool tied = key == kmax && best != 0ull;
+      const uint32_t bid = ~(uint32_t)best;
+      uint32_t win = __ballot_sync(0xffffffffu, tied);
+      if (__popc(win) > 1) {  // (warp-uniform) equal values: the lowest id, then the lowest lane
+        const uint32_t wid = __reduce_min_sync(0xffffffffu, tied ? bid : 0xffffffffu);
+        win = __ballot_sync(0xffffffffu, tied && bid == wid);
+      }
+      const int wl = win ? __ffs(win) - 1 : 0;
+      const uint32_t wid = __shfl_sync(0xffffffffu, bid, wl);
+      if (win != 0u && lane == k) {
+        out_id = (int32_t)wid;
+        out_v = key_value(kmax);
+        out_ok = true;
+      }
+      // the winner advances its list; every lane runs the same instructions
+      const bool me = win != 0u && lane == wl;
+      int h = 0;
+#pragma unroll
+      for (int m = 0; m < kMergeCache; ++m) h = (m == bm) ? hh[m] + 1 : h;
+      const bool more = me && h < 16;
+      const int p = lane + 32 * bm;
+      const float nv = sv[more ? p * 16 + h : 0];
+      const int32_t ni = si[more ? p * 16 + h : 0];
+      const uint64_t nk = more ? entry_key(nv, ni) : 0ull;
 #pragma unroll
       for (int m = 0; m < kMergeCache; ++m) {
-        if (m == bp) {  // (a register array indexed by a constant)
-          const int p = lane + 32 * m;
-          const int h = ++hh[m];
-          if (h < 16) {
-            hv[m] = sv[p * 16 + h];
-            hid[m] = si[p * 16 + h];
-          }
-        }
+        const bool upd = me && m == bm;
+        hh[m] = upd ? h : hh[m];
+        hk[m] = upd ? nk : hk[m];
       }
       pick();
-    });
+    }
   } else {
+    float bv = -INFINITY;
+    int32_t bid = 0x7fffffff;
+    int bp = -1;  // the lane's best list (-1: none left)
     auto rescan = [&]() {
       bv = -INFINITY;
       bid = 0x7fffffff;
@@ -125,10 +153,23 @@ __device__ __forceinline__ void warp_merge_lists(const float* sv, const int32_t*
       }
     };
     rescan();
-    round([&]() {
-      head[bp] += 1;
-      rescan();
-    });
+    for (int k = 0; k < K; ++k) {
+      const uint32_t key = bp >= 0 ? order_key(bv) : 0u;
+      const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
+      const bool tied = key == kmax && bp >= 0;
+      const uint32_t wid = __reduce_min_sync(0xffffffffu, tied ? (uint32_t)bid : 0xffffffffu);
+      const uint32_t win = __ballot_sync(0xffffffffu, tied && (uint32_t)bid == wid);
+      if (win != 0u && lane == k) {
+        out_id = (int32_t)wid;
+        out_v = key_value(kmax);
+        out_ok = true;
+      }
+      if (lane == __ffs(win) - 1) {
+        head[bp] += 1;
+        rescan();
+      }
+      __syncwarp();
+    }
   }
 }
 

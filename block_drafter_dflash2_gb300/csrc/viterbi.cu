@@ -378,27 +378,35 @@ __device__ void walk_warp0(SmemWalk& sw, int b, int T, int K, int flags, const S
     else sample_warp0(sw, b, T, K, sa, path_ids, path_idx, score);
   } else if (!greedy) {
     // Viterbi in fp32: delta_0 = lp_0 + tau_0(0, j); delta_t = lp_t + max_i (delta_{t-1}(i) + tau_t(i, j)).
-    // Each step, lane j loads its column of tau_t into registers and receives delta(i) by
-    // shuffles, so the max over i runs on registers (lowest i on ties: strict > in i order).
+    // Each step, lane j loads its column of tau_t into registers, receives delta(i) by shuffles
+    // and takes the max over i as a tree on registers: the right operand replaces the left only
+    // if strictly greater, so the lowest i wins ties (as a scan in i order with strict > would).
+    // Candidates i >= K enter as -inf and are never chosen over a live one.
     float delta = live ? sw.lp[0][j] + sw.tau[0][0][j] : -INFINITY;
     const int jc = j & (kKP - 1);  // lanes past the candidates read a valid column, unused
     for (int t = 1; t < T; ++t) {
-      float tc[kKP];
+      float v[kKP];
+      int ai[kKP];
 #pragma unroll
-      for (int i = 0; i < kKP; ++i) tc[i] = sw.tau[t][i][jc];
-      float best = __shfl_sync(0xffffffffu, delta, 0) + tc[0];
-      int arg = 0;
+      for (int i = 0; i < kKP; ++i) {
+        const float tc = sw.tau[t][i][jc];
+        const float di = __shfl_sync(0xffffffffu, delta, i);  // every lane, every i: no branch
+        v[i] = i < K ? di + tc : -INFINITY;
+        ai[i] = i;
+      }
 #pragma unroll
-      for (int i = 1; i < kKP; ++i) {
-        const float v = __shfl_sync(0xffffffffu, delta, i) + tc[i];
-        if (i < K && v > best) {
-          best = v;
-          arg = i;
+      for (int w = 1; w < kKP; w *= 2) {
+#pragma unroll
+        for (int a = 0; a < kKP; a += 2 * w) {
+          if (v[a + w] > v[a]) {
+            v[a] = v[a + w];
+            ai[a] = ai[a + w];
+          }
         }
       }
       if (live) {
-        delta = sw.lp[t][j] + best;
-        sw.bp[t][j] = (int8_t)arg;
+        delta = sw.lp[t][j] + v[0];
+        sw.bp[t][j] = (int8_t)ai[0];
       }
     }
     __syncwarp();
@@ -578,16 +586,23 @@ __global__ void __launch_bounds__(32 * kWarps)
         sw.lse[t] = lse;
         if (lse_out) lse_out[slot] = lse;
       }
-      warp_merge_lists(sv, si, head, parts, K, [&](int k, int32_t id, float v) {
-        const float lp = v - lse;
-        // every merged id indexes U and V below: a partial that held no column would carry an
-        // out-of-range id, so clamp (and flag) as for the caller's candidates
-        id = clamp_id(id, vocab, err, DFLASH2_DEVERR_CANDIDATE_RANGE);
-        sw.ids[t][k] = id;
-        sw.lp[t][k] = lp;
-        if (cand_ids) cand_ids[(size_t)slot * K + k] = id;
-        if (cand_lp) cand_lp[(size_t)slot * K + k] = lp;
-      });
+      {
+        int32_t id;
+        float v;
+        bool ok;
+        warp_merge_lists(sv, si, head, parts, K, id, v, ok);
+        if (ok) {  // lane k holds the k-th candidate
+          const int k = lane;
+          const float lp = v - lse;
+          // every merged id indexes U and V below: a partial that held no column would carry an
+          // out-of-range id, so clamp (and flag) as for the caller's candidates
+          id = clamp_id(id, vocab, err, DFLASH2_DEVERR_CANDIDATE_RANGE);
+          sw.ids[t][k] = id;
+          sw.lp[t][k] = lp;
+          if (cand_ids) cand_ids[(size_t)slot * K + k] = id;
+          if (cand_lp) cand_lp[(size_t)slot * K + k] = lp;
+        }
+      }
       __syncwarp();
       if (early) {
         // pad the slot (as pad_candidates does) and start its gathers into this warp's
