@@ -97,15 +97,17 @@ def test_planted_rows_reach_the_stated_peaks():
     sh = rc.shape
     planted = synth.planted_slots(rc)
     assert (planted >= 0).sum() >= 0.95 * planted.size
-    inp = synth.make_inputs(rc)
-    drawn = synth.normal(rc.seed, synth.TID_LM_HEAD, (sh.vocab, sh.hidden), rc.lm_head_std, "bf16")
+    inp = synth.make_inputs(rc, apply_planting=False)  # the rows as drawn
+    drawn = inp["lm_head"].copy()
+    synth.apply_planted_rows(rc, inp["lm_head"], planted)  # what make_inputs returns by default
     changed = np.nonzero(np.any(inp["lm_head"] != drawn, axis=1))[0]
     assert set(changed.tolist()) <= set(planted[planted >= 0].tolist())
     z = O.conv_chain(inp["hidden"], inp["conv_w"], "bf16", 16)
-    for b, t in ((0, 1), (3, 5), (6, 7)):
+    slots = ((0, 1), (3, 5), (6, 7))
+    ls = O.logits(np.stack([z[b, t] for b, t in slots]), inp["lm_head"]).astype(np.float64)  # one pass
+    for (b, t), l in zip(slots, ls):
         p = int(planted[b, t])
         assert p >= 0
-        l = O.logits(z[b, t][None], inp["lm_head"])[0].astype(np.float64)
         lse = l.max() + np.log(np.exp(l - l.max()).sum())
         assert abs(np.exp(l[p] - lse) - synth.PLANT_MASS) < 0.02
         assert int(np.argmax(l)) == p
