@@ -161,7 +161,7 @@ def test_conv_shift_limit_exact(B):
 # 256-column tiles in one chunk; 200 rows end in a ragged chunk
 @pytest.mark.parametrize("M,V,H", [(8, 248_320 // 8, 5120), (256, 30_011, 512), (1, 777, 64), (256, 16_400, 256),
                                    (256, 18_448, 256), (256, 19_472, 256), (512, 20_000, 256), (64, 9_001, 256),
-                                   (40, 5_000, 256), (200, 12_345, 256)])
+                                   (40, 5_000, 256), (200, 12_345, 256), (300, 7_777, 256)])
 def test_select_topk_step(M, V, H):
     rc = _recipe(batch=M, block=1, hidden=H, vocab=V, layers=0)
     sh = rc.shape
@@ -175,13 +175,15 @@ def test_select_topk_step(M, V, H):
     print(M, V, H, "near-tie rows", len(rep["near_tie_rows"]))
 
 
-def test_select_topk_exact_ties_take_lower_ids():
-    # every logit is an integer; many exact ties: the kept ids must be the lowest ids among ties
-    M, H, V, K = 4, 64, 5000, 16
+@pytest.mark.parametrize("M", [4, 160])
+def test_select_topk_exact_ties_take_lower_ids(M):
+    # every logit is an integer; many exact ties, within a column range and across ranges: the kept
+    # ids must be the lowest ids among ties (160 rows: the CTA-pair kernel, a ragged second chunk)
+    H, V, K = 64, 5000, 16
     z = np.zeros((M, H), np.float32)
-    z[np.arange(M), np.arange(M)] = 1.0
+    z[np.arange(M), np.arange(M) % 4] = 1.0
     W = np.zeros((V, H), np.float32)
-    W[:, :M] = (np.arange(V)[:, None] * np.array([3, 5, 7, 11])[None, :M]) % 13
+    W[:, :4] = (np.arange(V)[:, None] * np.array([3, 5, 7, 11])[None, :]) % 13
     zb = (z.view(np.uint32) >> 16).astype(np.uint16)
     Wb = (W.view(np.uint32) >> 16).astype(np.uint16)
     import block_drafter_dflash2_gb300 as df2
