@@ -565,7 +565,10 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 // ---------------------------------------------------------------------------
 // Epilogue 1: running top-16 (logit desc, id asc) and online log-sum-exp per row.
 // Each thread sees its row's columns in increasing id order, so inserting only values
-// strictly above the current 16th keeps equal logits in id order.
+// strictly above the current 16th keeps equal logits in id order. Per 32-column chunk, only the
+// chunk's columns above the 16th are visited, lowest first, one per iteration of a loop the warp
+// runs as often as its busiest lane needs (a per-column branch would make the warp run an
+// insertion for every column that any of its lanes keeps).
 // ---------------------------------------------------------------------------
 constexpr int kKeep = 16;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -641,9 +644,25 @@ struct EpiTopK {
       if (i < nvalid) acc += ex2_approx(fmaf(v[i], kLog2e, -mb));
     st.s += acc;
     if (cm > st.v[kKeep - 1]) {
+      uint32_t cand = 0;  // the chunk's columns above the 16th kept entry
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (i < nvalid && v[i] > st.v[kKeep - 1]) insert(st, v[i], col0 + i);
+      for (int i = 0; i < 32; ++i) cand |= (i < nvalid && v[i] > st.v[kKeep - 1]) ? (1u << i) : 0u;
+      while (cand) {
+        const int i = __ffs(cand) - 1;
+        cand &= cand - 1;
+        // v[i] without indexing registers: a tree on the bits of i
+        float t[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) t[k] = (i & 1) ? v[2 * k + 1] : v[2 * k];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) t[k] = (i & 2) ? t[2 * k + 1] : t[2 * k];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) t[k] = (i & 4) ? t[2 * k + 1] : t[2 * k];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) t[k] = (i & 8) ? t[2 * k + 1] : t[2 * k];
+        const float x = (i & 16) ? t[1] : t[0];
+        if (x > st.v[kKeep - 1]) insert(st, x, col0 + i);  // (the 16th rises as entries enter)
+      }
     }
   }
   static DF_DEV void finish(const State& st, const Params& p, int row, bool row_ok, int part) {
