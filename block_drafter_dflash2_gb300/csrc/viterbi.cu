@@ -58,6 +58,9 @@ struct SmemWalk {
   float lse[kMaxT];         // each slot's lse (for the score on raw logits)
   int8_t bp[kMaxT][kKP];
   int32_t anchor;
+  int32_t dry_ids[kMaxT];   // outputs of the fused kernel's dry run (discarded)
+  int32_t dry_idx[kMaxT];
+  float dry_score;
 };
 
 // Sampling parameters of the walk: u == nullptr is the Viterbi / greedy walk; otherwise a path
@@ -366,7 +369,7 @@ __device__ __forceinline__ float lse_sum(const SmemWalk& sw, int T) {
 }
 
 // The walk for sequence b on warp 0 (the other warps return before calling it).
-__device__ void walk_warp0(SmemWalk& sw, int b, int T, int K, int flags, const SampleArgs& sa,
+__device__ __noinline__ void walk_warp0(SmemWalk& sw, int b, int T, int K, int flags, const SampleArgs& sa,
                            int32_t* __restrict__ path_ids, int32_t* __restrict__ path_idx,
                            float* __restrict__ score) {
   const int lane = threadIdx.x & 31;
@@ -511,6 +514,46 @@ __host__ __device__ inline size_t select_region_stride(int parts) {
   return m > kTileStageBytes + kGateStageBytes ? m : kTileStageBytes + kGateStageBytes;
 }
 
+// lse and the K-way merge of one staged row (warp-wide), with the candidates written to sw and,
+// where the pointers are given, to global memory. Out of line, so that the dry call the fused
+// kernel makes while it waits for the LM head runs the same instructions as the real one.
+__device__ __noinline__ void merge_staged_row(const float* sv, const int32_t* si, const float2* sms, uint8_t* head,
+                                              int parts, int K, int vocab, int32_t* err, SmemWalk& sw, int t,
+                                              int slot, float* lse_out, int32_t* cand_ids, float* cand_lp) {
+  const int lane = threadIdx.x & 31;
+  float m = -INFINITY;
+  for (int p = lane; p < parts; p += 32) m = fmaxf(m, sms[p].x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float s = 0.f;
+  for (int p = lane; p < parts; p += 32)
+    if (sms[p].y > 0.f) s += sms[p].y * expf(sms[p].x - m);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  const float lse = m + logf(s);
+  if (lane == 0) {
+    sw.lse[t] = lse;
+    if (lse_out) lse_out[slot] = lse;
+  }
+  {
+    int32_t id;
+    float v;
+    bool ok;
+    warp_merge_lists(sv, si, head, parts, K, id, v, ok);
+    if (ok) {  // lane k holds the k-th candidate
+      const int k = lane;
+      const float lp = v - lse;
+      // every merged id indexes U and V below: a partial that held no column would carry an
+      // out-of-range id, so clamp (and flag) as for the caller's candidates
+      id = clamp_id(id, vocab, err, DFLASH2_DEVERR_CANDIDATE_RANGE);
+      sw.ids[t][k] = id;
+      sw.lp[t][k] = lp;
+      if (cand_ids) cand_ids[(size_t)slot * K + k] = id;
+      if (cand_lp) cand_lp[(size_t)slot * K + k] = lp;
+    }
+  }
+}
+
 template <bool kBf16>
 __global__ void __launch_bounds__(32 * kWarps)
     select_walk_kernel(const float* __restrict__ part_val, const int32_t* __restrict__ part_id,
@@ -547,6 +590,34 @@ __global__ void __launch_bounds__(32 * kWarps)
       cp_async_commit();
     }
   }
+  // Dry run while the LM head still runs (this kernel is its programmatic dependent, placed as
+  // the LM head's CTAs leave their SMs): the merge and the walk run once on placeholder lists in
+  // shared memory, every output kept in shared memory, so that the instructions of the real run
+  // below are in this SM's caches when the partials arrive (cold, each phase's first pass costs
+  // thousands of cycles of instruction fetch). Only for a few sequences: their CTAs take the first
+  // SMs the LM head frees, tens of microseconds before it ends; with many, the last ones placed
+  // would still be in the dry run when the partials are ready (measured: B = 1 -3 us, B = 32 +2.5).
+  if (gridDim.x <= kWarps) {
+    float* sv = reinterpret_cast<float*>(region + warp * wstride);
+    int32_t* si = reinterpret_cast<int32_t*>(sv + parts * 16);
+    float2* sms = reinterpret_cast<float2*>(si + parts * 16);
+    uint8_t* head = reinterpret_cast<uint8_t*>(sms + parts);
+    if (warp < T) {
+      for (int e = lane; e < parts * 16; e += 32) {
+        sv[e] = -(float)(e & 15);
+        si[e] = e;
+      }
+      for (int p = lane; p < parts; p += 32) {
+        sms[p] = make_float2(0.f, 1.f);
+        head[p] = 0;
+      }
+      __syncwarp();
+      merge_staged_row(sv, si, sms, head, parts, K, vocab, nullptr, sw, warp, 0, nullptr, nullptr, nullptr);
+    }
+    __syncthreads();
+    if (warp == 0) walk_warp0(sw, 0, T, K, walk_flags, sa, sw.dry_ids, sw.dry_idx, &sw.dry_score);
+    __syncthreads();
+  }
   // the partials are the LM head's output (launched as its programmatic dependent, the
   // prologue above overlaps its end)
   pdl_wait();
@@ -572,37 +643,7 @@ __global__ void __launch_bounds__(32 * kWarps)
       cp_async_commit();
       cp_async_wait_all();
       __syncwarp();
-      float m = -INFINITY;
-      for (int p = lane; p < parts; p += 32) m = fmaxf(m, sms[p].x);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      float s = 0.f;
-      for (int p = lane; p < parts; p += 32)
-        if (sms[p].y > 0.f) s += sms[p].y * expf(sms[p].x - m);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      const float lse = m + logf(s);
-      if (lane == 0) {
-        sw.lse[t] = lse;
-        if (lse_out) lse_out[slot] = lse;
-      }
-      {
-        int32_t id;
-        float v;
-        bool ok;
-        warp_merge_lists(sv, si, head, parts, K, id, v, ok);
-        if (ok) {  // lane k holds the k-th candidate
-          const int k = lane;
-          const float lp = v - lse;
-          // every merged id indexes U and V below: a partial that held no column would carry an
-          // out-of-range id, so clamp (and flag) as for the caller's candidates
-          id = clamp_id(id, vocab, err, DFLASH2_DEVERR_CANDIDATE_RANGE);
-          sw.ids[t][k] = id;
-          sw.lp[t][k] = lp;
-          if (cand_ids) cand_ids[(size_t)slot * K + k] = id;
-          if (cand_lp) cand_lp[(size_t)slot * K + k] = lp;
-        }
-      }
+      merge_staged_row(sv, si, sms, head, parts, K, vocab, err, sw, t, slot, lse_out, cand_ids, cand_lp);
       __syncwarp();
       if (early) {
         // pad the slot (as pad_candidates does) and start its gathers into this warp's
