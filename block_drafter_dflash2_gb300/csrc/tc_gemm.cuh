@@ -637,11 +637,12 @@ struct EpiTopK {
       st.s *= ex2_approx((st.m - cm) * kLog2e);
       st.m = cm;
     }
-    const float mb = st.m * kLog2e;
+    // exp(l - max) as 2^((l - max) log2 e): the difference first, so that the rounding of a large
+    // max times log2 e cannot leave a residual that overflows (a fused l log2 e - max log2 e would)
     float acc = 0.f;
 #pragma unroll
     for (int i = 0; i < 32; ++i)
-      if (i < nvalid) acc += ex2_approx(fmaf(v[i], kLog2e, -mb));
+      if (i < nvalid) acc += ex2_approx((v[i] - st.m) * kLog2e);
     st.s += acc;
     if (cm > st.v[kKeep - 1]) {
       uint32_t cand = 0;  // the chunk's columns above the 16th kept entry

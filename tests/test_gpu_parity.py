@@ -195,6 +195,33 @@ def test_select_topk_exact_ties_take_lower_ids(M):
     assert np.allclose(lse, O.logsumexp_rows(l32), atol=1e-4)
 
 
+@pytest.mark.parametrize("M", [4, 160])
+def test_select_topk_monotone_rows(M):
+    # rows whose logits rise with the column id (every column beats the kept 16th: the epilogue's
+    # candidate loop runs for all 32 columns of every chunk), fall with it (nothing enters after
+    # the first chunk), or are all equal (the lowest ids win every tie); exact in bf16:
+    # f(v) = (128 + v % 128) * 2^(v // 128) rises strictly with v
+    H, V, K = 64, 5000, 16
+    v = np.arange(V, dtype=np.float64)
+    f = (128 + v % 128) * np.exp2(v // 128)
+    W = np.zeros((V, H), np.float32)
+    W[:, 0], W[:, 1], W[:, 2] = f, -f, 1.0
+    z = np.zeros((M, H), np.float32)
+    z[np.arange(M), np.arange(M) % 3] = 1.0
+    zb = (z.view(np.uint32) >> 16).astype(np.uint16)
+    Wb = (W.view(np.uint32) >> 16).astype(np.uint16)
+    assert np.array_equal(O.widen(Wb)[:, 0], f)  # exactly representable
+    import block_drafter_dflash2_gb300 as df2
+    shape = df2.Shape.make(M, 1, H, V, K, 32, 0)
+    ids, lp, lse = P.run_topk(shape, P.dev(zb), P.dev(Wb))
+    l32 = O.logits(zb, Wb)
+    ids_o, _, _ = O.topk_rows(l32, K)
+    assert np.array_equal(ids, ids_o)
+    assert np.array_equal(ids[0], np.arange(V - 1, V - 1 - K, -1))
+    assert np.array_equal(ids[1], np.arange(K)) and np.array_equal(ids[2], np.arange(K))
+    assert np.allclose(lse, O.logsumexp_rows(l32), rtol=1e-5, atol=1e-4)
+
+
 @pytest.mark.parametrize("T,K,R", [(8, 16, 256), (1, 16, 256), (16, 4, 64), (32, 1, 16), (3, 16, 384)])
 def test_viterbi_step(T, K, R):
     rng = np.random.default_rng(T * 1000 + K * 10 + R)
