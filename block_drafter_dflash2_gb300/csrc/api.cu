@@ -43,47 +43,73 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return g_encode;
 }
 
-// Encoded maps are cached per host thread (16 entries, round robin): a call re-encodes only
-// maps it has not seen with the same base, shape and box. Encoding costs microseconds of host
-// time per map, which an eager caller pays on every call.
+// Encoded maps are cached per host thread (32 entries, round robin): a call re-encodes only
+// maps it has not seen with the same base, type, shape and box. Encoding costs microseconds of
+// host time per map, which an eager caller pays on every call.
 struct MapKey {
   const void* base;
-  uint64_t inner, rows;
-  uint32_t box_rows;
+  int dtype, rank, swizzle;
+  uint64_t dims[3];
+  uint32_t box[3];
 };
+constexpr int kMapCache = 32;
 struct MapCache {
-  MapKey key[16];
-  CUtensorMap map[16];
+  MapKey key[kMapCache];
+  CUtensorMap map[kMapCache];
   int n = 0, next = 0;
 };
 thread_local MapCache t_maps;
 
-// Row-major bf16 matrix [rows, inner] as a 2-D TMA map with a (64 x box_rows) box,
-// 128-byte swizzle, zero fill out of bounds.
-bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
-  for (int i = 0; i < t_maps.n; ++i) {
-    const MapKey& k = t_maps.key[i];
-    if (k.base == base && k.inner == inner && k.rows == rows && k.box_rows == box_rows) {
+bool same_key(const MapKey& a, const MapKey& b) {
+  if (a.base != b.base || a.dtype != b.dtype || a.rank != b.rank || a.swizzle != b.swizzle) return false;
+  for (int i = 0; i < a.rank; ++i)
+    if (a.dims[i] != b.dims[i] || a.box[i] != b.box[i]) return false;
+  return true;
+}
+
+// A dense row-major tensor (innermost dimension first in dims) as a tiled TMA map with the
+// given box, unit element strides and zero fill out of bounds; cached.
+bool encode_map(CUtensorMap* map, CUtensorMapDataType dtype, int esize, int rank, const void* base,
+                const uint64_t* dims, const uint32_t* box, CUtensorMapSwizzle swizzle) {
+  MapKey k{base, (int)dtype, rank, (int)swizzle, {0, 0, 0}, {0, 0, 0}};
+  for (int i = 0; i < rank; ++i) {
+    k.dims[i] = dims[i];
+    k.box[i] = box[i];
+  }
+  for (int i = 0; i < t_maps.n; ++i)
+    if (same_key(t_maps.key[i], k)) {
       *map = t_maps.map[i];
       return true;
     }
-  }
   auto enc = encoder();
   if (!enc) return false;
-  const cuuint64_t dims[2] = {inner, rows};
-  const cuuint64_t strides[1] = {inner * 2};
-  const cuuint32_t box[2] = {64, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  if (enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  cuuint64_t gdims[3], gstrides[2];
+  cuuint32_t gbox[3], estr[3] = {1, 1, 1};
+  uint64_t stride = (uint64_t)esize;
+  for (int i = 0; i < rank; ++i) {
+    gdims[i] = dims[i];
+    gbox[i] = box[i];
+    stride *= dims[i];
+    if (i + 1 < rank) gstrides[i] = stride;
+  }
+  if (enc(map, dtype, (cuuint32_t)rank, const_cast<void*>(base), gdims, gstrides, gbox, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return false;
   const int slot = t_maps.next;
-  t_maps.key[slot] = MapKey{base, inner, rows, box_rows};
+  t_maps.key[slot] = k;
   t_maps.map[slot] = *map;
-  t_maps.next = (slot + 1) % 16;
-  if (t_maps.n < 16) ++t_maps.n;
+  t_maps.next = (slot + 1) % kMapCache;
+  if (t_maps.n < kMapCache) ++t_maps.n;
   return true;
+}
+
+// Row-major bf16 matrix [rows, inner] as a 2-D TMA map with a (64 x box_rows) box,
+// 128-byte swizzle, zero fill out of bounds.
+bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  const uint64_t dims[2] = {inner, rows};
+  const uint32_t box[2] = {64, box_rows};
+  return encode_map(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 2, base, dims, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -242,15 +268,29 @@ dflash2_status_t run_conv(const Plan& p, const void* x, const void* conv_w, void
   if (p.NL == 0) return cuda_status(cudaMemcpyAsync(y, x, act, cudaMemcpyDeviceToDevice, s));
   if (p.bf16 && p.split) {
     const df::ConvSplitPlan& sp = p.split_plan;
-    CUtensorMap maps[7];
+    CUtensorMap maps[12];
     const void* srcs[3] = {x, w.conv0, w.conv1};
     for (int i = 0; i < 3; ++i)
       if (!encode_bf16_2d(&maps[2 * i], srcs[i], p.H, p.M, 128) ||
           !encode_bf16_2d(&maps[2 * i + 1], srcs[i], p.H, p.M, sp.a_tail_rows))
         return DFLASH2_ERR_CUDA;
     if (!encode_bf16_2d(&maps[6], conv_w, p.H, (uint64_t)p.NL * p.P, sp.Nt)) return DFLASH2_ERR_CUDA;
-    return cuda_status(df::launch_conv_splitk(sp, maps, x, w.conv0, w.conv1, y, w.conv_part, p.M, p.H, p.T, p.NL,
-                                              p.raw ? 1 : 0, w.bar, w.err, s));
+    const uint64_t pdims[3] = {(uint64_t)sp.Mp, (uint64_t)p.P, 2 * (uint64_t)sp.KS};
+    const uint32_t pst_box[3] = {(uint32_t)sp.br, (uint32_t)sp.Nt, 1};
+    const uint32_t pld_box[3] = {(uint32_t)sp.br, 2 * (uint32_t)sp.gc, (uint32_t)sp.KS};
+    if (!encode_map(&maps[7], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 3, w.conv_part, pdims, pst_box,
+                    CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_map(&maps[8], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 3, w.conv_part, pdims, pld_box,
+                    CU_TENSOR_MAP_SWIZZLE_NONE))
+      return DFLASH2_ERR_CUDA;
+    const uint64_t xdims[2] = {(uint64_t)p.H, (uint64_t)p.M};
+    const uint32_t xbox[2] = {(uint32_t)sp.xb, (uint32_t)sp.br};
+    for (int i = 0; i < 3; ++i)
+      if (!encode_map(&maps[9 + i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 2, srcs[i], xdims, xbox,
+                      CU_TENSOR_MAP_SWIZZLE_NONE))
+        return DFLASH2_ERR_CUDA;
+    return cuda_status(df::launch_conv_splitk(sp, maps, x, w.conv0, w.conv1, y, p.M, p.H, p.T, p.NL, p.raw ? 1 : 0,
+                                              w.bar, w.err, s));
   }
   if (p.bf16 && p.chain)
     return cuda_status(df::launch_conv_chain(p.chain_plan, x, conv_w, w.conv0, w.conv1, y, p.M, p.H, p.T, p.NL,

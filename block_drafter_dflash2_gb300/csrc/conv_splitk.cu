@@ -7,22 +7,26 @@
 //   A. TMA streams its (x rows, W rows) blocks of the slice through a 5-stage shared-memory
 //      ring (128-byte swizzle, K-major); one thread issues tcgen05.mma (M = 128, N = Nt,
 //      K = 16) into a TMEM accumulator; four epilogue warps (thread = TMEM lane = row) stage
-//      the fp32 partial taps in the idle operand ring as [tap][row], and all 256 threads
-//      write them to plane ks of [ks][q][m] with 16-byte stores (one scalar store per tap
-//      and row from the epilogue threads alone would be limited by the stores a warp may
-//      have in flight). Partials alternate between two sets of planes by layer parity.
+//      the fp32 partial taps in the idle operand ring as [tap][row], and one TMA store writes
+//      them to plane ks of [ks][q][m] (clipped at the tensor's edges). Partials alternate
+//      between two sets of planes by layer parity.
 //   grid barrier: every partial of the layer is written.
-//   B. The NT CTAs sharing (rt, ks) split the channel groups of the slice. For each of its
-//      (row, group) items a thread sums the group's two taps over the K-slices in slice
-//      order (up to 20 slices loaded before any is added, the rows' channels issued
-//      first), normalises them (softmax over the pair, unless raw), and writes
-//      y[m, c] = a * x_l[m-1, c] + b * x_l[m, c] for the group's 16 channels (x[-1] = 0 at
-//      each block start), rounded to bf16.
+//   B. The NT CTAs sharing (rt, ks) split the channel groups of the slice into contiguous
+//      ranges. In chunks that fit the idle ring, one 3-D TMA load brings the chunk's taps of
+//      every K-slice ([ks][tap][row]), and 2-D loads the tile's rows of the chunk's channels
+//      (when a CTA's groups make one chunk and shared memory has room, those row boxes have
+//      their own region and load while phase A runs: this CTA wrote them itself in the
+//      previous layer). From shared memory a thread per (row, group) sums the two taps over
+//      the K-slices in slice order, normalises them (softmax over the pair, unless raw), and
+//      writes y[m, c] = a * x_l[m-1, c] + b * x_l[m, c] for the group's 16 channels
+//      (x[-1] = 0 at each block start; the row above the tile, another tile's, comes from
+//      global memory into shared memory while the boxes land), rounded to bf16.
 //   sibling barrier: the NT CTAs of (rt, ks) wait for each other, since the next layer's A
 //      phase of each of them reads every channel of the slice for the tile's rows.
 // Each CTA reads only its K-slice of the rows and of its tap rows, so the per-layer traffic
-// is (M + P) * H * 2 bytes spread over the grid, plus the partial taps through L2; the older
-// chain kernel, where each CTA reads every hidden channel of its rows, suits small M only.
+// is (M + P) * H * 2 bytes spread over the grid, plus the partial taps through L2, moved by
+// the copy engine both ways; the older chain kernel, where each CTA reads every hidden channel
+// of its rows, suits small M only.
 // Every wait is bounded; on timeout the kernel sets DFLASH2_DEVERR_WAIT_TIMEOUT, lets copies
 // in flight land, frees TMEM and returns.
 #include <cuda_bf16.h>
@@ -33,6 +37,7 @@
 #include "kernels.h"
 #include "launch_util.h"
 #include "ptx.cuh"
+#include "tma_bulk.cuh"
 
 namespace df {
 
@@ -41,7 +46,7 @@ constexpr int kThreads = 256;
 constexpr int kStages = 5;
 constexpr uint32_t kABytes = 128 * 64 * 2;  // A region of a stage: the MMA reads 128 rows
 constexpr int kMaxTile = 160;                // widest tap tile
-constexpr int kC = 20;                       // K-slices whose partials a mix thread loads at once
+constexpr int kMaxSmem = 227 * 1024;         // dynamic shared memory a CTA may take
 
 struct SplitArgs {
   int M, H, T, NL, raw;
@@ -50,7 +55,13 @@ struct SplitArgs {
   int Nt;            // projection rows per tap tile (multiple of 16)
   int a_tail_rows;   // rows of the last row tile's TMA box (multiple of 8)
   int Mp;            // rows of a partial-tap plane (M rounded up to 4)
-  float* part;       // [2][KS][P][Mp] fp32 partial taps
+  int gc;            // channel groups per mix chunk
+  int br;            // rows of the partial-tap and row boxes: 128, or the rows of a single tile
+  int xb, nxs;       // channels per row box of the mix (br rows), row boxes per chunk
+  uint32_t pbox_bytes, xbox_bytes;  // a chunk's partial-tap box, one row box
+  int x_early;       // the row boxes have their own region and are loaded as the layer starts
+  uint32_t xoff;     // byte offset of the row boxes from the ring's start
+  uint32_t aboff;    // byte offset of the chunk's row above the tile ([gc][16] bf16) from the ring's start
   const __nv_bfloat16* x0;
   __nv_bfloat16* buf0;
   __nv_bfloat16* buf1;
@@ -59,29 +70,27 @@ struct SplitArgs {
   int32_t* err;
 };
 
-DF_DEV void tma_prefetch_2d(const CUtensorMap* map, int32_t c0, int32_t c1) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(c0), "r"(c1)
-               : "memory");
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
     conv_splitk_kernel(const __grid_constant__ CUtensorMap map_x0, const __grid_constant__ CUtensorMap map_x0t,
                        const __grid_constant__ CUtensorMap map_b0, const __grid_constant__ CUtensorMap map_b0t,
                        const __grid_constant__ CUtensorMap map_b1, const __grid_constant__ CUtensorMap map_b1t,
-                       const __grid_constant__ CUtensorMap map_w, const SplitArgs a) {
+                       const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_pst,
+                       const __grid_constant__ CUtensorMap map_pld, const __grid_constant__ CUtensorMap map_r0,
+                       const __grid_constant__ CUtensorMap map_r1, const __grid_constant__ CUtensorMap map_r2,
+                       const SplitArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(base);
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;
   uint64_t* drain = tfull + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* mixfull = drain + 1;  // a mix chunk's boxes have landed
+  uint64_t* rowsfull = mixfull + 1;  // the layer's row boxes have landed (x_early)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rowsfull + 1);
   volatile int* stop = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* consumed_s = stop + 1;  // ring loads the MMA thread has waited for
   uint8_t* ring = base + 1024;
-  float* stg = reinterpret_cast<float*>(ring);  // [Nt][128] fp32 tile of partials, in the idle ring
+  float* stg = reinterpret_cast<float*>(ring);  // [Nt][br] fp32 tile of partials, in the idle ring
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nt = blockIdx.x % a.NT;
@@ -96,7 +105,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int rows = min(128, a.M - rt * 128);
   const uint32_t tmem_cols = a.Nt <= 32 ? 32u : (a.Nt <= 64 ? 64u : (a.Nt <= 128 ? 128u : 256u));
   const uint32_t idesc = idesc_bf16_f32(128, a.Nt);
-  const size_t part_layer = (size_t)a.KS * a.P * a.Mp;
 
   pdl_launch_dependents();  // the LM head may start its prologue as SMs free up
   if (tid == 0) {
@@ -106,6 +114,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(tfull, 1);
     mbar_init(drain, 1);
+    mbar_init(mixfull, 1);
+    mbar_init(rowsfull, 1);
     *stop = 0;
     *consumed_s = 0;
     fence_barrier_init();
@@ -127,13 +137,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   uint32_t p_stage = 0, p_phase = 0, c_stage = 0, c_phase = 0;
-  int issued = 0;  // producer thread: ring loads issued
+  int issued = 0;     // producer thread: ring loads issued
+  uint32_t mixes = 0; // thread 0: mix chunks whose loads were issued
+  int rows_loaded = 0;  // thread 0: layers whose row boxes were loaded early
+  // this CTA's contiguous range of the slice's channel groups in the mix
+  const int g0 = kb0 * 4 + nt * ((kb1 - kb0) * 4) / a.NT, g1 = kb0 * 4 + (nt + 1) * ((kb1 - kb0) * 4) / a.NT;
+  const uint32_t xbox_tx = (uint32_t)(a.nxs * a.br * a.xb * 2);  // bytes of a chunk's row boxes
+  const uint32_t pbox_tx = (uint32_t)(a.br * 2 * a.gc * a.KS * 4);  // bytes of a chunk's partial-tap box
+  uint8_t* xboxes = ring + a.xoff;                                  // [nxs][br][xb] bf16
+  uint4* above = reinterpret_cast<uint4*>(ring + a.aboff);       // [gc][2] the row above the tile
   for (int l = 0; l < a.NL; ++l) {
     const CUtensorMap* mx = l == 0 ? (tail ? &map_x0t : &map_x0)
                                    : ((l - 1) % 2 == 0 ? (tail ? &map_b0t : &map_b0) : (tail ? &map_b1t : &map_b1));
+    const CUtensorMap* mrows = l == 0 ? &map_r0 : ((l - 1) % 2 == 0 ? &map_r1 : &map_r2);  // x_l, row boxes
     const __nv_bfloat16* xin = l == 0 ? a.x0 : ((l - 1) % 2 == 0 ? a.buf0 : a.buf1);
     __nv_bfloat16* xout = l == a.NL - 1 ? a.z : (l % 2 == 0 ? a.buf0 : a.buf1);
-    float* part = a.part + (size_t)(l & 1) * part_layer;
+    const int pset = (l & 1) * a.KS;  // this layer's set of partial-tap planes
 
     // ---- A. partial taps of the K-slice
     if (warp == 0) {
@@ -143,6 +162,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (l > 0) {
           asm volatile("fence.proxy.async.global;" ::: "memory");
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+        if (a.x_early) {
+          // the mix's rows of this tile for this CTA's groups: this CTA wrote them in the
+          // previous layer (the row above the tile, another tile's, is read in the mix itself)
+          mbar_arrive_expect_tx(rowsfull, xbox_tx);
+          for (int j = 0; j < a.nxs; ++j)
+            tma_load_2d(xboxes + (size_t)j * a.xbox_bytes, mrows, rowsfull, g0 * 16 + j * a.xb, rt * 128,
+                        l2_policy_evict_first());
+          ++rows_loaded;
         }
         const uint64_t pol = l2_policy_evict_last();
         for (int kb = kb0; kb < kb1; ++kb) {
@@ -200,95 +228,130 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c, v);
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-              if (c + i < a.Nt) stg[(c + i) * 128 + q * 32 + lane] = v[i];
+              if (c + i < a.Nt && q * 32 + lane < a.br) stg[(c + i) * a.br + q * 32 + lane] = v[i];
           }
         }
+        // generic writes that the TMA store below reads
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         tc_fence_before();
       }
     }
     __syncthreads();
-    // shared -> global by every thread, 16-byte stores: a warp instruction writes 32 x 4
-    // consecutive rows of one tap (a few stores per thread instead of one per tap and row)
-    {
-      const int r4n = (rows + 3) / 4;
-      const int ntaps = min(a.Nt, a.P - nt * a.Nt);
-      float* dst0 = part + ((size_t)ks * a.P + nt * a.Nt) * a.Mp + rt * 128;
-      for (int e = tid; e < ntaps * 32; e += kThreads) {
-        const int tap = e >> 5, r4 = e & 31;
-        if (r4 < r4n)
-          __stcg(reinterpret_cast<float4*>(dst0 + (size_t)tap * a.Mp + r4 * 4),
-                 *reinterpret_cast<const float4*>(stg + tap * 128 + r4 * 4));
-      }
-      // the next layer's TMA writes into this shared memory after the barriers
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    // staged partials -> plane ks of this layer's set: one TMA store of the [Nt][br] tile
+    // (taps past P and rows past the plane are not written); complete before the release
+    if (tid == 0 && *stop == 0) {
+      tma_store_3d(&map_pst, stg, rt * 128, nt * a.Nt, pset + ks);
+      bulk_commit();
+      bulk_wait_all();
+      asm volatile("fence.proxy.async.global;" ::: "memory");
     }
     if (!group_barrier(&a.bar[0], (unsigned)(l + 1), gridDim.x, a.err, stop)) break;
 
-    // ---- B. sum over the K-slices, normalise, mix
+    // ---- B. sum over the K-slices, normalise, mix: this CTA's groups [g0, g1) in chunks of
+    //      a.gc groups; the chunk's partial taps (and, unless loaded early, its row boxes) are
+    //      staged in the idle ring by TMA
     {
-      const int g_lo = kb0 * 4, ng = (kb1 - kb0) * 4;
-      const int my_ng = (ng - nt + a.NT - 1) / a.NT;  // groups g_lo + nt, g_lo + nt + NT, ...
-      const int items = rows * my_ng;
-      const size_t sstride = (size_t)a.P * a.Mp;
-      for (int it = tid; it < items; it += kThreads) {
-        const int r = it % rows, gi = it / rows;
-        const int g = g_lo + nt + gi * a.NT;
-        const int row = rt * 128 + r;
-        const int c0 = g * 16;
-        // the rows' channels first, so their loads are in flight with the partials'
-        const uint4* cur = reinterpret_cast<const uint4*>(xin + (size_t)row * a.H + c0);
-        uint4 cv[2] = {__ldcg(cur), __ldcg(cur + 1)};
-        uint4 pv[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
-        if (row % a.T != 0) {
-          pv[0] = __ldcg(cur - a.H / 8);  // the previous row
-          pv[1] = __ldcg(cur - a.H / 8 + 1);
+      const float* pbox = reinterpret_cast<const float*>(ring);  // [KS][2 gc][br] fp32
+      const int kstride = 2 * a.gc * a.br;
+      bool ok = true;
+      for (int c0 = g0; c0 < g1; c0 += a.gc) {
+        const int gn = min(a.gc, g1 - c0);
+        if (tid == 0) {
+          // the planes were written by other CTAs' TMA stores and the rows by generic stores;
+          // the ring last held generic accesses (the staged partials, the previous chunk)
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          mbar_arrive_expect_tx(mixfull, pbox_tx + (a.x_early ? 0u : xbox_tx));
+          tma_load_3d(ring, &map_pld, mixfull, rt * 128, 2 * c0, pset);
+          if (!a.x_early)
+            for (int j = 0; j < a.nxs; ++j)
+              tma_load_2d(xboxes + (size_t)j * a.xbox_bytes, mrows, mixfull, c0 * 16 + j * a.xb, rt * 128,
+                          l2_policy_evict_first());
+          ++mixes;
         }
-        const float* p0 = part + (size_t)(2 * g) * a.Mp + row;
-        // the partials of up to kC K-slices are loaded before any is added (one L2 round trip
-        // for every plan up to kC slices); they are added in slice order
-        float s0 = 0.f, s1 = 0.f;
-        for (int sb = 0; sb < a.KS; sb += kC) {
-          float v0[kC], v1[kC];
+        // the row above the tile (another tile's, written before the grid barrier) for the
+        // chunk's groups, one 16-byte load per thread while the boxes land; zero where the
+        // tile's first row starts a block
+        if (tid < 2 * gn) {
+          const int above_row = rt * 128 - 1;
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (above_row >= 0 && (above_row + 1) % a.T != 0)
+            v = __ldcg(reinterpret_cast<const uint4*>(xin + (size_t)above_row * a.H + (c0 + (tid >> 1)) * 16) +
+                       (tid & 1));
+          above[tid] = v;
+        }
+        if (tid == 0 && mbar_wait(mixfull, (mixes - 1) & 1u, a.err, stop) && a.x_early && c0 == g0)
+          mbar_wait(rowsfull, (uint32_t)(rows_loaded - 1) & 1u, a.err, stop);
+        __syncthreads();
+        if (*stop) {
+          ok = false;
+          break;
+        }
+        const int items = rows * gn;
+        for (int it = tid; it < items; it += kThreads) {
+          const int r = it % rows, gi = it / rows;
+          const int row = rt * 128 + r;
+          // the two taps summed over the K-slices in slice order, loads batched
+          const float* p0 = pbox + (size_t)(2 * gi) * a.br + r;
+          float s0 = 0.f, s1 = 0.f;
+          int k = 0;
+          for (; k + 8 <= a.KS; k += 8) {
+            float v0[8], v1[8];
 #pragma unroll
-          for (int j = 0; j < kC; ++j) {
-            if (sb + j < a.KS) {
-              v0[j] = __ldcg(p0 + (size_t)(sb + j) * sstride);
-              v1[j] = __ldcg(p0 + (size_t)(sb + j) * sstride + a.Mp);
+            for (int j = 0; j < 8; ++j) {
+              v0[j] = p0[(size_t)(k + j) * kstride];
+              v1[j] = p0[(size_t)(k + j) * kstride + a.br];
             }
-          }
 #pragma unroll
-          for (int j = 0; j < kC; ++j) {
-            if (sb + j < a.KS) {
+            for (int j = 0; j < 8; ++j) {
               s0 += v0[j];
               s1 += v1[j];
             }
           }
-        }
-        float wa, wb;
-        if (a.raw) {
-          wa = s0;
-          wb = s1;
-        } else {
-          const float mx = fmaxf(s0, s1);
-          const float e0 = expf(s0 - mx), e1 = expf(s1 - mx);
-          const float inv = 1.f / (e0 + e1);
-          wa = e0 * inv;
-          wb = e1 * inv;
-        }
-        uint4 out[2];
-        const __nv_bfloat162* c2 = reinterpret_cast<const __nv_bfloat162*>(cv);
-        const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(pv);
-        __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(out);
+          for (; k < a.KS; ++k) {
+            s0 += p0[(size_t)k * kstride];
+            s1 += p0[(size_t)k * kstride + a.br];
+          }
+          float wa, wb;
+          if (a.raw) {
+            wa = s0;
+            wb = s1;
+          } else {
+            const float mx = fmaxf(s0, s1);
+            const float e0 = expf(s0 - mx), e1 = expf(s1 - mx);
+            const float inv = 1.f / (e0 + e1);
+            wa = e0 * inv;
+            wb = e1 * inv;
+          }
+          // box row r is row `row`; the previous row is box row r - 1, or for the tile's first
+          // row the last row of the tile above (x[-1] = 0 at each block start)
+          const int sub = (gi * 16) / a.xb, cc = (gi * 16) % a.xb;  // the boxes start at group c0
+          const __nv_bfloat16* xs = reinterpret_cast<const __nv_bfloat16*>(xboxes + (size_t)sub * a.xbox_bytes);
+          const uint4* cur = reinterpret_cast<const uint4*>(xs + (size_t)r * a.xb + cc);
+          uint4 cv[2] = {cur[0], cur[1]};
+          uint4 pv[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+          if (row % a.T != 0) {
+            const uint4* prv = r > 0 ? reinterpret_cast<const uint4*>(xs + (size_t)(r - 1) * a.xb + cc) : above + 2 * gi;
+            pv[0] = prv[0];
+            pv[1] = prv[1];
+          }
+          uint4 out[2];
+          const __nv_bfloat162* c2 = reinterpret_cast<const __nv_bfloat162*>(cv);
+          const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(pv);
+          __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(out);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const float2 cf = __bfloat1622float2(c2[k]);
-          const float2 pf = __bfloat1622float2(p2[k]);
-          o2[k] = __floats2bfloat162_rn(fmaf(wa, pf.x, wb * cf.x), fmaf(wa, pf.y, wb * cf.y));
+          for (int q = 0; q < 8; ++q) {
+            const float2 cf = __bfloat1622float2(c2[q]);
+            const float2 pf = __bfloat1622float2(p2[q]);
+            o2[q] = __floats2bfloat162_rn(fmaf(wa, pf.x, wb * cf.x), fmaf(wa, pf.y, wb * cf.y));
+          }
+          uint4* dst = reinterpret_cast<uint4*>(xout + (size_t)row * a.H + (c0 + gi) * 16);
+          dst[0] = out[0];
+          dst[1] = out[1];
         }
-        uint4* dst = reinterpret_cast<uint4*>(xout + (size_t)row * a.H + c0);
-        dst[0] = out[0];
-        dst[1] = out[1];
+        __syncthreads();  // the next chunk's copies overwrite the boxes
       }
+      if (!ok) break;
     }
     if (l + 1 < a.NL && !group_barrier(&a.bar[1 + sib], (unsigned)(l + 1), (unsigned)a.NT, a.err, stop)) break;
   }
@@ -298,6 +361,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     for (int i = *consumed_s; i < issued; ++i)
       if (!mbar_wait(&full[i % kStages], (uint32_t)(i / kStages) & 1u, a.err, nullptr)) break;
+    if (mixes > 0) mbar_wait(mixfull, (mixes - 1) & 1u, a.err, nullptr);  // the last mix chunk's copies
+    if (rows_loaded > 0) mbar_wait(rowsfull, (uint32_t)(rows_loaded - 1) & 1u, a.err, nullptr);
+    bulk_wait_all();                                                     // and the partials' store
   }
   if (warp == 1) {
     if (lane == 0) {
@@ -335,12 +401,44 @@ bool conv_splitk_plan(int M, int H, int NL, int sms, ConvSplitPlan* out) {
   out->smem = splitk_smem(Nt);
   out->Mp = (M + 3) / 4 * 4;
   out->part_bytes = 2 * (size_t)KS * P * out->Mp * sizeof(float);
-  return true;
+  // box rows: a single row tile's (a multiple of 8), else 128 (the last tile's box reads zeros
+  // past the tensor)
+  const int br = RT == 1 ? out->a_tail_rows : 128;
+  out->br = br;
+  // mix chunks: the most channel groups whose partial taps (2 per group, every K-slice, br rows
+  // of fp32) and row boxes (br rows of 16 channels) fit the operand ring
+  const size_t ring = (size_t)kStages * (kABytes + ((Nt * 128 + 1023) & ~1023));
+  const int ng_max = 4 * ((H / 64 + KS - 1) / KS);  // groups of the widest K-slice
+  const int g_cta = (ng_max + NT - 1) / NT;          // groups of one CTA, at most
+  int gc = g_cta < 128 ? g_cta : 128;
+  for (; gc >= 1; --gc) {
+    const int xb = 16 * (gc < 8 ? gc : 8);
+    const int nxs = (16 * gc + xb - 1) / xb;
+    const size_t xbox = (size_t)br * xb * 2;                                // a multiple of 256
+    const size_t pbox = ((size_t)br * 2 * gc * KS * 4 + 127) & ~size_t(127);  // 128-B aligned
+    if (pbox + nxs * xbox <= ring) {
+      out->gc = gc;
+      out->xb = xb;
+      out->nxs = nxs;
+      out->pbox_bytes = (uint32_t)pbox;
+      out->xbox_bytes = (uint32_t)xbox;
+      // one chunk per CTA and room past the ring: the row boxes get their own region, loaded
+      // while the layer's taps are contracted
+      const size_t above = ((size_t)gc * 32 + 127) & ~size_t(127);  // the row above the tile
+      out->x_early = gc == g_cta && out->smem + nxs * xbox + above <= (size_t)kMaxSmem;
+      out->xoff = out->x_early ? (uint32_t)ring : (uint32_t)pbox;
+      if (out->x_early) out->smem += nxs * xbox;
+      out->aboff = (uint32_t)(out->smem - 2048);  // past the ring and the early row boxes
+      out->smem += above;
+      return out->smem <= (size_t)kMaxSmem;
+    }
+  }
+  return false;
 }
 
 cudaError_t launch_conv_splitk(const ConvSplitPlan& pl, const CUtensorMap* maps, const void* x, void* buf0,
-                               void* buf1, void* z, float* part, int M, int H, int T, int NL, int raw,
-                               unsigned* bar_counts, int32_t* err, cudaStream_t s) {
+                               void* buf1, void* z, int M, int H, int T, int NL, int raw, unsigned* bar_counts,
+                               int32_t* err, cudaStream_t s) {
   static unsigned char smem_done[64];
   cudaError_t e = smem_opt_in(reinterpret_cast<const void*>(conv_splitk_kernel), smem_done);
   if (e != cudaSuccess) return e;
@@ -359,7 +457,15 @@ cudaError_t launch_conv_splitk(const ConvSplitPlan& pl, const CUtensorMap* maps,
   a.Nt = pl.Nt;
   a.a_tail_rows = pl.a_tail_rows;
   a.Mp = pl.Mp;
-  a.part = part;
+  a.gc = pl.gc;
+  a.br = pl.br;
+  a.xb = pl.xb;
+  a.nxs = pl.nxs;
+  a.pbox_bytes = pl.pbox_bytes;
+  a.xbox_bytes = pl.xbox_bytes;
+  a.x_early = pl.x_early;
+  a.xoff = pl.xoff;
+  a.aboff = pl.aboff;
   a.x0 = reinterpret_cast<const __nv_bfloat16*>(x);
   a.buf0 = reinterpret_cast<__nv_bfloat16*>(buf0);
   a.buf1 = reinterpret_cast<__nv_bfloat16*>(buf1);
@@ -377,7 +483,7 @@ cudaError_t launch_conv_splitk(const ConvSplitPlan& pl, const CUtensorMap* maps,
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, conv_splitk_kernel, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6],
-                         a);
+                         maps[7], maps[8], maps[9], maps[10], maps[11], a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -50,14 +50,23 @@ struct ConvSplitPlan {
   int Mp;              // rows of a partial-tap plane (M rounded up to 4)
   int grid;            // RT * NT * KS CTAs
   size_t smem;         // dynamic shared memory per CTA
-  size_t part_bytes;   // workspace for the partial taps
+  size_t part_bytes;   // workspace for the partial taps, [2][KS][H/8][Mp] fp32
+  int gc;              // channel groups per mix chunk
+  int br;              // rows of the partial-tap and row boxes (128, or a single tile's rows)
+  int xb, nxs;         // channels of a mix row box (br rows), row boxes per chunk
+  uint32_t pbox_bytes, xbox_bytes;  // a chunk's partial-tap box; one row box
+  int x_early;         // row boxes in their own region, loaded as each layer starts
+  uint32_t xoff;       // byte offset of the row boxes from the operand ring
+  uint32_t aboff;      // byte offset of the row above the tile ([gc][16] bf16) from the ring
 };
 bool conv_splitk_plan(int M, int H, int NL, int sms, ConvSplitPlan* out);
-// maps: x (128-row box), x (tail box), buf0, buf0 tail, buf1, buf1 tail, all layers' weights
-// [NL * H/8, H] (Nt-row box). Zeroes the barrier counters first.
+// maps: 0-5 the x operand (128-row box, tail box) of x, buf0, buf1 (128-B swizzle, 64 columns);
+// 6 all layers' weights [NL * H/8, H] (Nt-row box); 7 the partial taps [2 KS][H/8][Mp] fp32
+// with a (br, Nt, 1) box, 8 the same with a (br, 2 gc, KS) box; 9-11 the mix row boxes
+// (xb columns, br rows, no swizzle) of x, buf0, buf1. Zeroes the barrier counters first.
 cudaError_t launch_conv_splitk(const ConvSplitPlan& pl, const CUtensorMap* maps, const void* x, void* buf0,
-                               void* buf1, void* z, float* part, int M, int H, int T, int NL, int raw,
-                               unsigned* bar_counts, int32_t* err, cudaStream_t s);
+                               void* buf1, void* z, int M, int H, int T, int NL, int raw, unsigned* bar_counts,
+                               int32_t* err, cudaStream_t s);
 
 // fp32 instantiations (small sizes).
 cudaError_t launch_conv_layer_f32(const float* x, const float* w, float* y, int M, int H, int T, int raw,

@@ -88,11 +88,11 @@ def _conv_parity(sh, inp):
     return P.check_conv_layers(inp["hidden"], inp["conv_w"], sh.dtype, sh.taps, zl, z, ref_chain=ref)
 
 
-# 8 and 16 rows run the chain kernel that reads whole rows per CTA; 40, 96 and 160 rows the
-# split-K chain (one row tile; one tile; two tiles with a 32-row tail)
+# 8 and 16 rows run the chain kernel that reads whole rows per CTA; 40, 96, 160 and 256 rows
+# the split-K chain (one row tile; one tile; two tiles with a 32-row tail; two full tiles)
 @pytest.mark.parametrize("layers,raw,batch", [(1, False, 1), (5, False, 1), (5, False, 2), (1, False, 5),
                                               (5, False, 5), (1, True, 5), (1, False, 12), (5, False, 12),
-                                              (1, True, 12), (5, False, 20)])
+                                              (1, True, 12), (5, False, 20), (1, True, 20), (5, False, 32)])
 def test_conv_step(layers, raw, batch):
     rc = _recipe(batch=batch, block=8, hidden=5120, vocab=64, layers=layers)
     sh = rc.shape
@@ -105,6 +105,15 @@ def test_conv_step(layers, raw, batch):
 
 def test_conv_step_block16_many_rows():
     rc = _recipe(batch=40, block=16, hidden=1024, vocab=64, layers=5)
+    sh = rc.shape
+    inp = synth.make_inputs(rc)
+    print(_conv_parity(sh, inp))
+
+
+def test_conv_step_mix_chunks():
+    # 4864 rows at hidden 2560: 38 row tiles of two tap tiles leave two K-slices of 20 blocks, so
+    # each CTA's 40 channel groups are mixed in two chunks whose row boxes share the operand ring
+    rc = _recipe(batch=608, block=8, hidden=2560, vocab=64, layers=2)
     sh = rc.shape
     inp = synth.make_inputs(rc)
     print(_conv_parity(sh, inp))
@@ -125,11 +134,14 @@ def test_conv_step_few_rows(batch, block, hidden, layers, raw):
     print(_conv_parity(sh, inp))
 
 
-@pytest.mark.parametrize("batch,block,hidden,layers", [(11, 12, 512, 3), (1, 8, 1088, 2), (4, 5, 1088, 2)])
+@pytest.mark.parametrize("batch,block,hidden,layers", [(11, 12, 512, 3), (1, 8, 1088, 2), (4, 5, 1088, 2),
+                                                      (6, 8, 128, 3), (20, 15, 768, 2)])
 def test_conv_step_tile_edges(batch, block, hidden, layers):
     # 132 rows with block 12: sequences cross the 128-row tile boundary and the last tile has
     # 4 rows; hidden 1088 (not a multiple of 256) takes the per-layer path at 8 rows and the
-    # split-K chain at 20 rows of block 5, where 136 taps per layer fill a 144-row tap tile
+    # split-K chain at 20 rows of block 5, where 136 taps per layer fill a 144-row tap tile;
+    # 48 rows at hidden 128 (two K blocks), 300 rows at hidden 768 (three row tiles crossed by
+    # sequences of 15)
     rc = _recipe(batch=batch, block=block, hidden=hidden, vocab=64, layers=layers)
     sh = rc.shape
     inp = synth.make_inputs(rc)
