@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           asm volatile("fence.proxy.async.global;" ::: "memory");
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         }
-        if (a.x_early) {
+        if (a.x_early && g1 > g0) {  // (the mix waits for these rows only when it has groups)
           // the mix's rows of this tile for this CTA's groups: this CTA wrote them in the
           // previous layer (the row above the tile, another tile's, is read in the mix itself)
           mbar_arrive_expect_tx(rowsfull, xbox_tx);
